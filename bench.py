@@ -1,0 +1,477 @@
+#!/usr/bin/env python
+"""Benchmark of one mixed continuous-batching attention step on GB300.
+
+A step is one pass of the whole path over one iteration's synthetic batch:
+KV append of the iteration's new rows (``mb_kv_append``), planning with the
+one host->device upload of the work lists (``mb_attn_plan``) and the
+attention of every request (``mb_attn_forward``: split-KV / cascade kernel,
+LSE combine, tcgen05 prefill kernel). Inputs are resident in HBM; between
+timed steps the L2 is flushed by writing a 256 MiB buffer (outside the timed
+events). Each step is timed with CUDA events on the launching stream.
+
+Default workload: the Llama-2-7B-shaped layer of one ORCA iteration (a
+4096-row prefill beside decodes at kv 1500 and 1700; 32 heads, head dim 128,
+page 16). The metric is Q rows per second; the dominant kernel's roofline,
+the end-to-end number through host buffers and the CPU oracle's rate on a
+bounded sample are reported beside it, one JSON line on stdout.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+Multi-GPU (torchrun): independent replicas, one per rank, no collective on
+the data path; ranks meet only for the barrier and the max-over-ranks time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from continuous_batching_paged_varlen_gb300 import counters as C  # noqa: E402
+from continuous_batching_paged_varlen_gb300 import workloads as W  # noqa: E402
+
+METRIC = "mixed-iteration attention Q rows/s; achieved HBM TB/s or tensor-pipe % of peak"
+UNIT = "Q rows/s"
+DEFAULT_WORKLOAD = "llama2_7b_orca_iteration"
+PREFILL_MIN_ROWS = 16  # the planner's default split between the two kernels
+FLUSH_BYTES = 256 << 20
+STAGES = ["decode", "combine", "prefill"]
+KERNEL_SOURCES = {"prefill": "prefill.cu", "decode": "decode.cu", "combine": "combine.cu"}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.ORDER)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="budget of the oracle CPU baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, local, world
+
+
+# --------------------------------------------------------------- peaks
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# --------------------------------------------------------------- algorithmic work
+
+def stage_work(w):
+    """Algorithmic FLOPs and bytes of the two attention kernels' request sets."""
+    s = w.spec
+    reqs = w.requests
+    m = reqs[:, 1] - reqs[:, 0]
+    pre = reqs[m >= PREFILL_MIN_ROWS]
+    dec_idx = np.nonzero((m > 0) & (m < PREFILL_MIN_ROWS))[0]
+    dec = reqs[dec_idx]
+    out = {}
+    out["prefill_flops"] = C.attention_flops(pre, s.n_q_heads, s.head_dim) if len(pre) else 0
+    out["prefill_bytes"] = (C.attention_bytes(pre, w.block_table[m >= PREFILL_MIN_ROWS],
+                                              s.n_q_heads, s.n_kv_heads, s.head_dim,
+                                              s.page_size) if len(pre) else 0)
+    out["decode_flops"] = C.attention_flops(dec, s.n_q_heads, s.head_dim) if len(dec) else 0
+    out["decode_bytes"] = (C.attention_bytes(dec, w.block_table[dec_idx], s.n_q_heads,
+                                             s.n_kv_heads, s.head_dim, s.page_size)
+                           if len(dec) else 0)
+    out["total_flops"] = C.attention_flops(reqs, s.n_q_heads, s.head_dim)
+    out["total_bytes"] = C.attention_bytes(reqs, w.block_table, s.n_q_heads, s.n_kv_heads,
+                                           s.head_dim, s.page_size)
+    out["append_bytes"] = C.append_bytes(w.total_q, s.n_kv_heads, s.head_dim)
+    return out
+
+
+def source_hash(kernel):
+    path = os.path.join(ROOT, "continuous_batching_paged_varlen_gb300", "csrc",
+                        KERNEL_SOURCES[kernel])
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
+    the current source of that kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{kernel}:{workload}")
+    if not e or e.get("source_sha256_16") != source_hash(kernel):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names[1:], parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        loaded = [x for x in sm if x > 0.5 * (mx or max(sm))] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- CPU oracle timing
+
+def time_oracle_sample(w, budget_s, rotate=0):
+    """Time the fp64 oracle on a bounded sample of workload w; returns
+    (Q rows/s extrapolated to the whole workload, description, seconds)."""
+    from oracle import attention as OA  # the oracle is only used on this leg
+
+    s = w.spec
+    g = s.n_q_heads // s.n_kv_heads
+    t_total_est = 0.0
+    spent = 0.0
+    parts = []
+    order = sorted(range(w.n_requests), key=lambda r: int(w.requests[r, 1] - w.requests[r, 0]))
+    for r in order:
+        qs, qe, kv = [int(x) for x in w.requests[r]]
+        if qe == qs:
+            continue
+        k, v = w.logical_kv(r)
+        k = k.to("cpu").double().numpy()
+        v = v.to("cpu").double().numpy()
+        q = w.q[qs:qe].to("cpu").double().numpy()
+        heads_done = 0
+        t_req = 0.0
+        for i in range(s.n_q_heads):
+            h = (i + rotate) % s.n_q_heads
+            kh = h // g
+            t0 = time.perf_counter()
+            OA.attend(q[:, h:h + 1], k[:, kh:kh + 1], v[:, kh:kh + 1], s.scale)
+            dt = time.perf_counter() - t0
+            t_req += dt
+            heads_done += 1
+            spent += dt
+            if spent > budget_s:
+                break
+        t_total_est += t_req * s.n_q_heads / heads_done
+        parts.append(f"req{r}(q{qe - qs},kv{kv}):{heads_done}/{s.n_q_heads} heads")
+        if spent > budget_s:
+            # requests not reached: extrapolate with the per-pair cost seen so far
+            done_pairs = sum(C.pairs(int(w.requests[x, 1] - w.requests[x, 0]), int(w.requests[x, 2]))
+                             for x in order[:order.index(r) + 1])
+            all_pairs = sum(C.pairs(int(a[1] - a[0]), int(a[2])) for a in w.requests)
+            if done_pairs < all_pairs:
+                t_total_est *= all_pairs / done_pairs
+                parts.append(f"rest extrapolated by pairs ({done_pairs}/{all_pairs})")
+            break
+    rate = w.total_q / t_total_est if t_total_est > 0 else 0.0
+    return rate, "; ".join(parts), spent
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# --------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    w = W.make_workload(args.workload, device="cpu")
+    per_step = max(1.0, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    rates = []
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        rate, desc, spent = time_oracle_sample(w, per_step, rotate=i)
+        if i >= args.warmup:
+            rates.append(rate)
+    value = statistics.median(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.total_q / value * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"per step ~{per_step:.0f} s of fp64 oracle work: {desc}; "
+                                   "rate extrapolated to every head / request"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(w):
+    s = w.spec
+    return {"workload": s.name, "description": s.description, "q_rows": w.total_q,
+            "requests": w.n_requests, "n_q_heads": s.n_q_heads, "n_kv_heads": s.n_kv_heads,
+            "head_dim": s.head_dim, "page_size": s.page_size,
+            "l2": "flushed between timed steps (256 MiB write, outside the events)",
+            "step": "mb_kv_append + mb_attn_plan (host + 1 H2D) + mb_attn_forward"}
+
+
+# --------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+
+    from continuous_batching_paged_varlen_gb300 import binding as B
+    from continuous_batching_paged_varlen_gb300 import build as build_mod
+
+    rank, local, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build_mod.build()
+    B.lib()
+
+    w = W.make_workload(args.workload, device=dev)
+    s = w.spec
+    cfg = B.config(s.n_q_heads, s.n_kv_heads, s.head_dim, s.page_size, w.num_pages,
+                   w.block_table.shape[1], s.scale or 0.0)
+    shape = (w.num_pages, s.n_kv_heads, s.page_size, s.head_dim)
+    kc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    n_hist = int(w.hist_requests[:, 1].max()) if w.n_requests else 0
+    if n_hist:
+        hs = B.slot_mapping(w.hist_requests, w.block_table, cfg, n_hist)
+        B.kv_append(kc, vc, w.k_hist, w.v_hist, torch.from_numpy(hs).to(dev), cfg, status)
+    slots = torch.from_numpy(B.slot_mapping(w.requests, w.block_table, cfg, w.total_q)).to(dev)
+    bt_dev = torch.from_numpy(np.ascontiguousarray(w.block_table)).to(dev)
+    q, k_new, v_new = w.q, w.k_new, w.v_new
+    out = torch.empty((w.total_q, s.n_q_heads, s.head_dim), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.total_q, s.n_q_heads), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    probe = B.Plan(w.requests, w.block_table, cfg, device=dev)
+    info = probe.info.as_dict()
+    ws = probe.workspace
+    probe.close()
+    launches_per_step = 1 + info["n_launches"]
+
+    def step(stage_events=None):
+        B.kv_append(kc, vc, k_new, v_new, slots, cfg, status)
+        plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=ws)
+        plan.forward(q, kc, vc, bt_dev, out, lse, events=stage_events)
+        plan.close()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(STAGES))]
+           for _ in range(K)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step(sev[i])
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    stage_ms = {}
+    for si, name in enumerate(STAGES):
+        if info[{"decode": "n_decode_items", "combine": "n_combine",
+                 "prefill": "n_prefill_items"}[name]] > 0:
+            stage_ms[name] = statistics.mean(
+                sev[i][2 * si].elapsed_time(sev[i][2 * si + 1]) for i in range(K))
+    ms_step = statistics.mean(step_ms)
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * w.total_q * K / (total_ms / 1e3)
+    dev_status = int(ws[:4].view(torch.int32).item()) | int(status.item())
+
+    # ---- roofline of the dominant kernel
+    peaks = load_peaks()
+    work = stage_work(w)
+    dominant = max(stage_ms, key=stage_ms.get) if stage_ms else None
+    roof = None
+    if dominant == "prefill":
+        t = stage_ms["prefill"] / 1e3
+        ach = work["prefill_flops"] / t / 1e12
+        roof = {"kernel": "prefill_kernel (tcgen05)", "bound": "tensor", "achieved": ach,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16_tflops"],
+                "peak_kind": f"bf16 dense burst ({peaks['source']})",
+                "algorithmic_per_launch": work["prefill_flops"],
+                "traffic": recorded_traffic("prefill", s.name)}
+    elif dominant == "decode":
+        t = stage_ms["decode"] / 1e3
+        ach = work["decode_bytes"] / t / 1e9
+        roof = {"kernel": "splitkv_kernel", "bound": "hbm", "achieved": ach,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+                "peak_kind": f"HBM copy ({peaks['source']})",
+                "algorithmic_per_launch": work["decode_bytes"],
+                "traffic": recorded_traffic("decode", s.name)}
+
+    # ---- end to end through host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq = q.cpu().pin_memory()
+        hk = k_new.cpu().pin_memory()
+        hv = v_new.cpu().pin_memory()
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            B.kv_append(kc, vc, dk, dv, slots, cfg, status)
+            plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=ws)
+            plan.forward(dq, kc, vc, bt_dev, out, lse)
+            plan.close()
+            hout.copy_(out, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_ms = []
+        for i in range(K):
+            flush.zero_()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            e2e_step()
+            torch.cuda.synchronize()
+            e_ms.append((time.perf_counter() - t0) * 1e3)
+        h2d = (hq.numel() + hk.numel() + hv.numel()) * 2 + info["metadata_bytes"]
+        d2h = hout.numel() * 2 + hlse.numel() * 4
+        e2e = {"value": world * w.total_q / (statistics.mean(e_ms) / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": statistics.mean(e_ms),
+               "timing": "host wall clock around each step, synchronised; inputs copied from "
+                         "pinned host memory, output and LSE copied back"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, desc, spent = time_oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{spent:.1f} s of fp64 oracle work: {desc}; extrapolated to every "
+                         "head / request of the workload"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**workload_config(w), "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+        "stages_ms": stage_ms,
+        "achieved": {"attention_tflops": work["total_flops"] / (ms_step / 1e3) / 1e12,
+                     "attention_hbm_gbs": work["total_bytes"] / (ms_step / 1e3) / 1e9,
+                     "algorithmic_flops_per_step": work["total_flops"],
+                     "algorithmic_bytes_per_step": work["total_bytes"] + work["append_bytes"]},
+        "plan": info, "device_status": dev_status, "wall_s_timed_region": wall,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0 if dev_status == 0 else 3
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,269 @@
+"""Thin ctypes binding of ``libmb.so`` (the C ABI in ``include/mb.h``).
+
+Only argument marshalling happens here: every step of the attention path
+runs in the library's CUDA kernels. The library is loaded lazily by
+``lib()``, which raises when it has not been built -- there is no fallback.
+PyTorch supplies device memory and streams; tensors are passed by pointer.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmb.so")
+
+MB_OK = 0
+STATUS_NAMES = {0: "MB_OK", 1: "MB_ERR_INVALID_ARG", 2: "MB_ERR_SHAPE",
+                3: "MB_ERR_UNSUPPORTED", 4: "MB_ERR_WORKSPACE", 5: "MB_ERR_CUDA",
+                6: "MB_ERR_TIMEOUT", 7: "MB_ERR_DEVICE_INDEX"}
+MB_ERR_TIMEOUT = 6
+MB_ERR_DEVICE_INDEX = 7
+STAGE_DECODE, STAGE_COMBINE, STAGE_PREFILL, NUM_STAGES = 0, 1, 2, 3
+
+
+class MBError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+
+
+class Request(ctypes.Structure):
+    _fields_ = [("q_start", ctypes.c_int32), ("q_end", ctypes.c_int32),
+                ("kv_length", ctypes.c_int32)]
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32), ("max_blocks_per_req", ctypes.c_int32),
+                ("scale", ctypes.c_float)]
+
+
+class PlanOptions(ctypes.Structure):
+    _fields_ = [("prefill_min_rows", ctypes.c_int32), ("kv_chunk", ctypes.c_int32),
+                ("disable_cascade", ctypes.c_int32), ("target_ctas", ctypes.c_int32)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("n_decode_items", ctypes.c_int32), ("n_decode_rows", ctypes.c_int32),
+                ("n_prefill_items", ctypes.c_int32), ("n_combine", ctypes.c_int32),
+                ("n_partials", ctypes.c_int32), ("n_cascade_groups", ctypes.c_int32),
+                ("cascade_keys", ctypes.c_int32), ("kv_chunk", ctypes.c_int32),
+                ("total_q", ctypes.c_int32), ("n_launches", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_size_t), ("metadata_bytes", ctypes.c_size_t)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+_lib = None
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_pi32 = ctypes.POINTER(ctypes.c_int32)
+
+
+def lib():
+    """The loaded library; raises if ``libmb.so`` is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (there is no fallback path)")
+    L = ctypes.CDLL(LIB_PATH)
+    L.mb_abi_version.restype = _i32
+    L.mb_status_string.restype = ctypes.c_char_p
+    L.mb_status_string.argtypes = [ctypes.c_int]
+    L.mb_slot_mapping.restype = ctypes.c_int
+    L.mb_slot_mapping.argtypes = [_vp, _i32, _vp, ctypes.POINTER(Config), _vp, _i32]
+    L.mb_kv_append.restype = ctypes.c_int
+    L.mb_kv_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, ctypes.POINTER(Config), _vp, _vp]
+    L.mb_attn_plan.restype = ctypes.c_int
+    L.mb_attn_plan.argtypes = [_vp, _i32, _vp, ctypes.POINTER(Config), _vp,
+                               ctypes.POINTER(ctypes.c_size_t), _vp, ctypes.POINTER(_vp)]
+    L.mb_attn_plan_ex.restype = ctypes.c_int
+    L.mb_attn_plan_ex.argtypes = [_vp, _i32, _vp, ctypes.POINTER(Config),
+                                  ctypes.POINTER(PlanOptions), _vp,
+                                  ctypes.POINTER(ctypes.c_size_t), _vp, ctypes.POINTER(_vp)]
+    L.mb_attn_plan_host.restype = ctypes.c_int
+    L.mb_attn_plan_host.argtypes = [_vp, _i32, _vp, ctypes.POINTER(Config),
+                                    ctypes.POINTER(PlanOptions), ctypes.POINTER(_vp)]
+    L.mb_attn_forward.restype = ctypes.c_int
+    L.mb_attn_forward.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    L.mb_attn_forward_timed.restype = ctypes.c_int
+    L.mb_attn_forward_timed.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    L.mb_plan_info.restype = ctypes.c_int
+    L.mb_plan_info.argtypes = [_vp, ctypes.POINTER(PlanInfo)]
+    L.mb_plan_export_metadata.restype = ctypes.c_int
+    L.mb_plan_export_metadata.argtypes = [_vp, _vp, ctypes.c_size_t]
+    L.mb_plan_layout.restype = ctypes.c_int
+    L.mb_plan_layout.argtypes = [_vp, ctypes.POINTER(ctypes.c_size_t)]
+    L.mb_attn_destroy.restype = ctypes.c_int
+    L.mb_attn_destroy.argtypes = [_vp]
+    _lib = L
+    return L
+
+
+def check(status: int, what: str):
+    if status != MB_OK:
+        raise MBError(status, what)
+
+
+def config(n_q_heads, n_kv_heads, head_dim, page_size, num_pages, max_blocks_per_req,
+           scale=0.0) -> Config:
+    return Config(n_q_heads, n_kv_heads, head_dim, page_size, num_pages,
+                  max_blocks_per_req, float(scale or 0.0))
+
+
+def options(prefill_min_rows=0, kv_chunk=0, disable_cascade=0, target_ctas=0) -> PlanOptions:
+    return PlanOptions(prefill_min_rows, kv_chunk, disable_cascade, target_ctas)
+
+
+def _host_i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _stream_ptr(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def slot_mapping(requests, block_table, cfg: Config, total_q: int) -> np.ndarray:
+    """``mb_slot_mapping``: int32 slot of every flat new row (-1 if uncovered)."""
+    reqs = _host_i32(requests).reshape(-1, 3)
+    bt = _host_i32(block_table)
+    out = np.empty(max(total_q, 1), dtype=np.int32)
+    check(lib().mb_slot_mapping(reqs.ctypes.data, reqs.shape[0], bt.ctypes.data,
+                                ctypes.byref(cfg), out.ctypes.data, total_q),
+          "mb_slot_mapping")
+    return out[:total_q]
+
+
+def kv_append(k_cache, v_cache, k_new, v_new, slots, cfg: Config, status=None, stream=None):
+    """``mb_kv_append`` on torch tensors (``slots``: int32 device tensor)."""
+    T = int(slots.numel())
+    check(lib().mb_kv_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+                             _ptr(slots), T, ctypes.byref(cfg), _ptr(status),
+                             _stream_ptr(stream) if T else None),
+          "mb_kv_append")
+
+
+class HostPlan:
+    """A plan built on the host only (``mb_attn_plan_host``), for inspection."""
+
+    def __init__(self, requests, block_table, cfg: Config, opts: Optional[PlanOptions] = None):
+        self.reqs = _host_i32(requests).reshape(-1, 3)
+        self.bt = _host_i32(block_table)
+        self.cfg = cfg
+        h = ctypes.c_void_p()
+        check(lib().mb_attn_plan_host(self.reqs.ctypes.data, self.reqs.shape[0],
+                                      self.bt.ctypes.data, ctypes.byref(cfg),
+                                      ctypes.byref(opts) if opts else None, ctypes.byref(h)),
+              "mb_attn_plan_host")
+        self._h = h
+
+    @property
+    def info(self) -> PlanInfo:
+        inf = PlanInfo()
+        check(lib().mb_plan_info(self._h, ctypes.byref(inf)), "mb_plan_info")
+        return inf
+
+    def layout(self):
+        arr = (ctypes.c_size_t * 6)()
+        check(lib().mb_plan_layout(self._h, arr), "mb_plan_layout")
+        return list(arr)
+
+    def metadata(self) -> bytes:
+        n = self.info.metadata_bytes
+        buf = (ctypes.c_uint8 * n)()
+        check(lib().mb_plan_export_metadata(self._h, buf, n), "mb_plan_export_metadata")
+        return bytes(buf)
+
+    def close(self):
+        if self._h:
+            lib().mb_attn_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Plan:
+    """``mb_attn_plan`` + a caller-owned (torch) workspace; ``forward`` runs
+    ``mb_attn_forward`` on the given stream."""
+
+    def __init__(self, requests, block_table, cfg: Config, device="cuda",
+                 opts: Optional[PlanOptions] = None, stream=None, workspace=None):
+        import torch
+        self.reqs = _host_i32(requests).reshape(-1, 3)
+        self.bt = _host_i32(block_table)
+        self.cfg = cfg
+        L = lib()
+        nbytes = ctypes.c_size_t(0)
+        check(L.mb_attn_plan_ex(self.reqs.ctypes.data, self.reqs.shape[0], self.bt.ctypes.data,
+                                ctypes.byref(cfg), ctypes.byref(opts) if opts else None, None,
+                                ctypes.byref(nbytes), None, None),
+              "mb_attn_plan (size query)")
+        self.workspace_bytes = int(nbytes.value)
+        if workspace is None or workspace.numel() < self.workspace_bytes:
+            workspace = torch.empty(max(self.workspace_bytes, 256), dtype=torch.uint8,
+                                    device=device)
+        self.workspace = workspace
+        h = ctypes.c_void_p()
+        nb = ctypes.c_size_t(workspace.numel())
+        check(L.mb_attn_plan_ex(self.reqs.ctypes.data, self.reqs.shape[0], self.bt.ctypes.data,
+                                ctypes.byref(cfg), ctypes.byref(opts) if opts else None,
+                                _ptr(workspace), ctypes.byref(nb), _stream_ptr(stream),
+                                ctypes.byref(h)),
+              "mb_attn_plan")
+        self._h = h
+
+    @property
+    def info(self) -> PlanInfo:
+        inf = PlanInfo()
+        check(lib().mb_plan_info(self._h, ctypes.byref(inf)), "mb_plan_info")
+        return inf
+
+    def forward(self, q, k_cache, v_cache, block_table_dev, out, lse=None, stream=None,
+                events=None):
+        L = lib()
+        if events is None:
+            st = L.mb_attn_forward(self._h, _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(block_table_dev), _ptr(out), _ptr(lse),
+                                   _stream_ptr(stream))
+        else:
+            arr = (ctypes.c_void_p * (2 * NUM_STAGES))(
+                *[None if e is None else ctypes.c_void_p(e.cuda_event) for e in events])
+            st = L.mb_attn_forward_timed(self._h, _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                         _ptr(block_table_dev), _ptr(out), _ptr(lse),
+                                         _stream_ptr(stream), arr)
+        check(st, "mb_attn_forward")
+
+    def device_status(self) -> int:
+        """Device error flags of this plan's workspace (synchronises)."""
+        return int(self.workspace[:4].view(dtype=__import__("torch").int32).item())
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().mb_attn_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

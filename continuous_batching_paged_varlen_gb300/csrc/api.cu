@@ -1,0 +1,175 @@
+// extern "C" entry points that launch work: mb_kv_append and the two forward
+// calls. Argument checks happen here on the host; nothing is enqueued when a
+// check fails.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "../../include/mb.h"
+#include "kernels.h"
+#include "mb_internal.h"
+#include "plan_impl.h"
+
+using namespace mb;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 128-byte-swizzled bf16 tensor map; dims/strides innermost first, strides
+// for dims 1.. in bytes.
+bool make_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+              const cuuint64_t* strides, const cuuint32_t* box) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t elem[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
+                  dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace
+
+extern "C" {
+
+mb_status_t mb_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                         const int32_t* slot_mapping, int32_t T, const mb_config_t* cfg,
+                         int32_t* status_dev, cudaStream_t stream) {
+  mb_status_t st = validate_config(cfg);
+  if (st != MB_OK) return st;
+  if (T < 0) return MB_ERR_INVALID_ARG;
+  if (T == 0) return MB_OK;
+  if (!k_cache || !v_cache || !k_new || !v_new || !slot_mapping) return MB_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 3) ||
+      (reinterpret_cast<uintptr_t>(status_dev) & 3))
+    return MB_ERR_INVALID_ARG;
+  cudaError_t e = launch_kv_append(k_cache, v_cache, k_new, v_new, slot_mapping, T,
+                                   cfg->n_kv_heads, cfg->head_dim, cfg->page_size,
+                                   cfg->num_pages, status_dev, stream);
+  return e == cudaSuccess ? MB_OK : MB_ERR_CUDA;
+}
+
+mb_status_t mb_attn_forward_timed(const mb_plan_t* plan, const void* q, const void* k_cache,
+                                  const void* v_cache, const int32_t* block_table_dev,
+                                  void* out, float* lse, cudaStream_t stream,
+                                  cudaEvent_t* events) {
+  if (!plan || !plan->workspace) return MB_ERR_INVALID_ARG;
+  const PlanDevice& d = plan->dev;
+  if (d.total_q == 0) return MB_OK;
+  if (!q || !k_cache || !v_cache || !block_table_dev || !out) return MB_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3) ||
+      (reinterpret_cast<uintptr_t>(block_table_dev) & 3))
+    return MB_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(plan->workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  const float scale_log2 = d.scale * kLog2e;
+  auto rec = [&](int stage, int which) {
+    if (events && events[2 * stage + which]) cudaEventRecord(events[2 * stage + which], stream);
+  };
+  cudaError_t e = cudaSuccess;
+
+  if (d.n_decode_items > 0) {
+    DecodeArgs a;
+    a.items = reinterpret_cast<const DecodeItem*>(ws + d.off_decode_items);
+    a.rows = reinterpret_cast<const RowDesc*>(ws + d.off_rows);
+    a.n_items = d.n_decode_items;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_table = block_table_dev;
+    a.max_blocks = d.max_blocks;
+    a.n_q_heads = d.n_q_heads;
+    a.n_kv_heads = d.n_kv_heads;
+    a.head_dim = d.head_dim;
+    a.page_size = d.page_size;
+    a.num_pages = d.num_pages;
+    a.scale_log2 = scale_log2;
+    a.out = out;
+    a.lse = lse;
+    a.part_o = reinterpret_cast<float*>(ws + d.off_part_o);
+    a.part_lse = reinterpret_cast<float*>(ws + d.off_part_lse);
+    a.status = status;
+    rec(MB_STAGE_DECODE, 0);
+    e = launch_decode(a, stream);
+    rec(MB_STAGE_DECODE, 1);
+    if (e != cudaSuccess) return MB_ERR_CUDA;
+  }
+  if (d.n_combine > 0) {
+    rec(MB_STAGE_COMBINE, 0);
+    e = launch_combine(reinterpret_cast<const CombineEntry*>(ws + d.off_combine), d.n_combine,
+                       reinterpret_cast<const float*>(ws + d.off_part_o),
+                       reinterpret_cast<const float*>(ws + d.off_part_lse), d.head_dim,
+                       d.n_q_heads, out, lse, stream);
+    rec(MB_STAGE_COMBINE, 1);
+    if (e != cudaSuccess) return MB_ERR_CUDA;
+  }
+  if (d.n_prefill_items > 0) {
+    CUtensorMap qm, km, vm;
+    const cuuint64_t qdims[3] = {(cuuint64_t)d.head_dim, (cuuint64_t)d.n_q_heads,
+                                 (cuuint64_t)d.total_q};
+    const cuuint64_t qstr[2] = {(cuuint64_t)d.head_dim * 2,
+                                (cuuint64_t)d.n_q_heads * d.head_dim * 2};
+    const cuuint32_t qbox[3] = {64, 1, (cuuint32_t)kPrefillTileM};
+    const cuuint64_t kvdims[2] = {(cuuint64_t)d.head_dim,
+                                  (cuuint64_t)d.num_pages * d.n_kv_heads * d.page_size};
+    const cuuint64_t kvstr[1] = {(cuuint64_t)d.head_dim * 2};
+    const cuuint32_t kvbox[2] = {64, (cuuint32_t)d.page_size};
+    if (!make_map(&qm, q, 3, qdims, qstr, qbox) || !make_map(&km, k_cache, 2, kvdims, kvstr, kvbox) ||
+        !make_map(&vm, v_cache, 2, kvdims, kvstr, kvbox))
+      return MB_ERR_CUDA;
+    PrefillArgs a;
+    a.items = reinterpret_cast<const PrefillItem*>(ws + d.off_prefill_items);
+    a.n_items = d.n_prefill_items;
+    a.block_table = block_table_dev;
+    a.max_blocks = d.max_blocks;
+    a.n_q_heads = d.n_q_heads;
+    a.n_kv_heads = d.n_kv_heads;
+    a.head_dim = d.head_dim;
+    a.page_size = d.page_size;
+    a.num_pages = d.num_pages;
+    a.scale_log2 = scale_log2;
+    a.out = out;
+    a.lse = lse;
+    a.status = status;
+    a.q_map = &qm;
+    a.k_map = &km;
+    a.v_map = &vm;
+    rec(MB_STAGE_PREFILL, 0);
+    e = launch_prefill(a, stream);
+    rec(MB_STAGE_PREFILL, 1);
+    if (e != cudaSuccess) return MB_ERR_CUDA;
+  }
+  return MB_OK;
+}
+
+mb_status_t mb_attn_forward(const mb_plan_t* plan, const void* q, const void* k_cache,
+                            const void* v_cache, const int32_t* block_table_dev, void* out,
+                            float* lse, cudaStream_t stream) {
+  return mb_attn_forward_timed(plan, q, k_cache, v_cache, block_table_dev, out, lse, stream,
+                               nullptr);
+}
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// Launchers of the device kernels (host side; defined next to each kernel).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+#include <stdint.h>
+
+#include "mb_internal.h"
+
+namespace mb {
+
+// KV append scatter (kv_append.cu).
+cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new,
+                             const void* v_new, const int32_t* slots, int32_t T,
+                             int32_t n_kv_heads, int32_t head_dim, int32_t page_size,
+                             int32_t num_pages, int32_t* status, cudaStream_t s);
+
+// Split-KV / cascade kernel (decode.cu): partial or final rows.
+struct DecodeArgs {
+  const DecodeItem* items;
+  const RowDesc* rows;
+  int32_t n_items;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  int32_t max_blocks, n_q_heads, n_kv_heads, head_dim, page_size, num_pages;
+  float scale_log2;  // softmax scale * log2(e)
+  void* out;
+  float* lse;        // nullable
+  float* part_o;
+  float* part_lse;   // log2 domain
+  int32_t* status;
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+// LSE merge of partials (combine.cu).
+cudaError_t launch_combine(const CombineEntry* entries, int32_t n, const float* part_o,
+                           const float* part_lse, int32_t head_dim, int32_t n_q_heads,
+                           void* out, float* lse, cudaStream_t s);
+
+// tcgen05 prefill kernel (prefill.cu).
+struct PrefillArgs {
+  const PrefillItem* items;
+  int32_t n_items;
+  const int32_t* block_table;
+  int32_t max_blocks, n_q_heads, n_kv_heads, head_dim, page_size, num_pages;
+  float scale_log2;
+  void* out;
+  float* lse;
+  int32_t* status;
+  const CUtensorMap* q_map;  // host copies, passed by value to the kernel
+  const CUtensorMap* k_map;
+  const CUtensorMap* v_map;
+};
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
+
+}  // namespace mb

@@ -1,0 +1,84 @@
+// Internal types shared by the host planner and the kernels.
+//
+// The planner (plan.cpp) turns the iteration's triples and block tables into
+// flat work lists that it uploads into the caller's workspace with one
+// host->device copy. Workspace layout (offsets in bytes, each region
+// 256-byte aligned):
+//
+//   [0, 256)            status word (int32, device error flags) + padding
+//   decode_items        DecodeItem[n_decode_items]    (split-KV / cascade CTAs)
+//   rows                RowDesc[n_decode_rows]        (query rows of those CTAs)
+//   prefill_items       PrefillItem[n_prefill_items]  (tensor-core prefill CTAs)
+//   combine             CombineEntry[n_combine]       (rows merged from partials)
+//   ---- metadata above is uploaded; scratch below is written by kernels ----
+//   part_lse            float[n_partials]             (log2-domain LSE per partial)
+//   part_o              float[n_partials * head_dim]  (normalised partial outputs)
+#pragma once
+
+#include <stdint.h>
+
+namespace mb {
+
+constexpr int kStatusBytes = 256;
+constexpr int kRowsPerDecodeItem = 8;   // query rows one split-KV CTA owns
+constexpr int kPrefillTileM = 128;      // query rows per prefill CTA
+constexpr int kPrefillTileN = 128;      // keys per prefill KV tile
+
+// One CTA of the split-KV kernel: query rows (all of one KV head) against
+// the key range [k_begin, k_end) of one block-table row.
+struct DecodeItem {
+  int32_t bt_row;     // block-table row that addresses the keys
+  int32_t kv_head;
+  int32_t k_begin;    // logical key range
+  int32_t k_end;
+  int32_t row_begin;  // first RowDesc
+  int32_t n_rows;     // <= kRowsPerDecodeItem
+  int32_t pad0, pad1;
+};
+
+struct RowDesc {
+  int32_t q_index;  // flat token row of q / out
+  int32_t q_head;
+  int32_t vis_end;  // keys j < vis_end are visible to this row (S0 + i + 1)
+  int32_t dst;      // >= 0: partial slot; < 0: final row, write out / lse
+};
+
+// One CTA of the prefill kernel: up to kPrefillTileM consecutive new rows of
+// one request and one query head, against keys [0, n_kv_tiles * TileN).
+struct PrefillItem {
+  int32_t req;         // block-table row
+  int32_t q_head;
+  int32_t q_row0;      // flat token row of the tile's first row
+  int32_t n_rows;      // valid rows in the tile
+  int32_t s0;          // cached columns of the request
+  int32_t i0;          // index of the tile's first row among the request's new rows
+  int32_t kv_length;
+  int32_t n_kv_tiles;  // ceil(min(kv_length, s0 + i0 + n_rows) / TileN)
+};
+
+struct CombineEntry {
+  int32_t q_index;
+  int32_t q_head;
+  int32_t slot_begin;  // partial slots [slot_begin, slot_begin + n_slots)
+  int32_t n_slots;
+};
+
+static_assert(sizeof(DecodeItem) == 32, "layout");
+static_assert(sizeof(RowDesc) == 16, "layout");
+static_assert(sizeof(PrefillItem) == 32, "layout");
+static_assert(sizeof(CombineEntry) == 16, "layout");
+
+// Everything a forward needs from a plan.
+struct PlanDevice {
+  int32_t n_decode_items, n_decode_rows, n_prefill_items, n_combine, n_partials;
+  int32_t n_q_heads, n_kv_heads, head_dim, page_size, num_pages, max_blocks;
+  int32_t total_q;
+  float scale;
+  size_t off_decode_items, off_rows, off_prefill_items, off_combine, off_part_lse,
+      off_part_o;
+  size_t metadata_bytes, workspace_bytes;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace mb

@@ -1,0 +1,569 @@
+// Host planner: validation, request classification, shared-prefix grouping,
+// split-KV chunking and workspace layout for one iteration.
+//
+// The triple (q_start, q_end, kv_length) and the two-block mask follow
+// "ORCA and chunked prefill", sections 2 and 4; pages shared between
+// requests and the "load a common block once for every request that uses
+// it" cascade follow "How To Scale Your Model notes (7-8)", section 3.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "../../include/mb.h"
+#include "mb_internal.h"
+#include "plan_impl.h"
+
+using namespace mb;
+
+namespace {
+
+constexpr int kDefaultPrefillMinRows = 16;
+constexpr int kDefaultTargetCtas = 4 * 152;
+constexpr int kMinChunk = 256;
+
+bool is_pow2_in(int v, int lo, int hi) {
+  return v >= lo && v <= hi && (v & (v - 1)) == 0;
+}
+
+}  // namespace
+
+namespace mb {
+
+mb_status_t validate_config(const mb_config_t* cfg) {
+  if (!cfg) return MB_ERR_INVALID_ARG;
+  if (cfg->n_q_heads <= 0 || cfg->n_kv_heads <= 0 || cfg->num_pages <= 0 ||
+      cfg->max_blocks_per_req <= 0 || cfg->page_size <= 0 || cfg->head_dim <= 0)
+    return MB_ERR_SHAPE;
+  if (cfg->n_q_heads % cfg->n_kv_heads != 0) return MB_ERR_SHAPE;
+  if (!(cfg->scale >= 0.0f) || !isfinite(cfg->scale)) return MB_ERR_INVALID_ARG;
+  if (cfg->head_dim != 64 && cfg->head_dim != 128) return MB_ERR_UNSUPPORTED;
+  if (!is_pow2_in(cfg->page_size, 16, 128)) return MB_ERR_UNSUPPORTED;
+  // element offsets of the caches must fit the kernels' 64-bit math and the
+  // tensor-map row coordinate (int32)
+  int64_t rows = (int64_t)cfg->num_pages * cfg->n_kv_heads * cfg->page_size;
+  if (rows >= ((int64_t)1 << 31)) return MB_ERR_UNSUPPORTED;
+  return MB_OK;
+}
+
+mb_status_t validate_requests(const mb_request_t* reqs, int32_t n,
+                              const int32_t* bt, const mb_config_t* cfg,
+                              int32_t* total_q_out) {
+  if (n < 0) return MB_ERR_INVALID_ARG;
+  if (n > 0 && (!reqs || !bt)) return MB_ERR_INVALID_ARG;
+  const int ps = cfg->page_size;
+  int32_t total_q = 0;
+  std::vector<std::pair<int32_t, int32_t>> ranges;
+  for (int32_t r = 0; r < n; ++r) {
+    const mb_request_t& q = reqs[r];
+    if (q.q_start < 0 || q.q_end < q.q_start || q.kv_length < 0) return MB_ERR_SHAPE;
+    const int32_t m = q.q_end - q.q_start;
+    if (m > q.kv_length) return MB_ERR_SHAPE;
+    if (m == 0) continue;
+    const int64_t blocks = ((int64_t)q.kv_length + ps - 1) / ps;
+    if (blocks > cfg->max_blocks_per_req) return MB_ERR_SHAPE;
+    const int32_t* row = bt + (size_t)r * cfg->max_blocks_per_req;
+    for (int64_t b = 0; b < blocks; ++b)
+      if (row[b] < 0 || row[b] >= cfg->num_pages) return MB_ERR_SHAPE;
+    ranges.push_back({q.q_start, q.q_end});
+    total_q = std::max(total_q, q.q_end);
+  }
+  std::sort(ranges.begin(), ranges.end());
+  for (size_t i = 1; i < ranges.size(); ++i)
+    if (ranges[i].first < ranges[i - 1].second) return MB_ERR_SHAPE;
+  if ((int64_t)total_q * cfg->n_q_heads * cfg->head_dim >= ((int64_t)1 << 40))
+    return MB_ERR_UNSUPPORTED;
+  *total_q_out = total_q;
+  return MB_OK;
+}
+
+namespace {
+
+struct Sequence {       // one key range walked by split-KV CTAs
+  int32_t bt_row;
+  int32_t k_begin, k_end;
+  std::vector<int32_t> members;  // requests whose rows attend to it
+  bool shared;
+};
+
+}  // namespace
+
+mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
+                       const int32_t* bt, const mb_config_t* cfg,
+                       const mb_plan_options_t* opts, mb_plan* plan) {
+  mb_status_t st = validate_config(cfg);
+  if (st != MB_OK) return st;
+  int32_t total_q = 0;
+  st = validate_requests(reqs, n, bt, cfg, &total_q);
+  if (st != MB_OK) return st;
+
+  mb_plan_options_t o = {};
+  if (opts) o = *opts;
+  if (o.kv_chunk < 0 || (o.kv_chunk % 64) != 0 || o.target_ctas < 0)
+    return MB_ERR_INVALID_ARG;
+  const int prefill_min = o.prefill_min_rows == 0 ? kDefaultPrefillMinRows
+                                                  : o.prefill_min_rows;
+  const int target = o.target_ctas ? o.target_ctas : kDefaultTargetCtas;
+
+  const int Hq = cfg->n_q_heads, Hkv = cfg->n_kv_heads, g = Hq / Hkv;
+  const int ps = cfg->page_size, D = cfg->head_dim;
+  const int mb = cfg->max_blocks_per_req;
+
+  std::vector<int32_t> prefill_reqs, decode_reqs;
+  for (int32_t r = 0; r < n; ++r) {
+    const int32_t m = reqs[r].q_end - reqs[r].q_start;
+    if (m == 0) continue;
+    if (prefill_min > 0 && m >= prefill_min)
+      prefill_reqs.push_back(r);
+    else
+      decode_reqs.push_back(r);
+  }
+
+  // ---- shared-prefix groups among split-KV requests -------------------
+  std::vector<int32_t> own_begin(n, 0);
+  std::vector<Sequence> seqs;
+  int32_t n_groups = 0, cascade_keys = 0;
+  if (!o.disable_cascade) {
+    std::map<int32_t, std::vector<int32_t>> by_first;
+    for (int32_t r : decode_reqs) {
+      const int32_t s0 = reqs[r].kv_length - (reqs[r].q_end - reqs[r].q_start);
+      if (s0 >= ps) by_first[bt[(size_t)r * mb]].push_back(r);
+    }
+    for (auto& kv : by_first) {
+      std::vector<int32_t>& mem = kv.second;
+      if (mem.size() < 2) continue;
+      // longest run of leading blocks that every member maps to the same
+      // physical page and that lies wholly inside every member's cache
+      int32_t L = 0;
+      for (;; ++L) {
+        bool ok = true;
+        // (L + 1) * ps <= s0 <= kv_length keeps L inside every member's
+        // validated block-table entries; check it before reading entry L
+        for (int32_t r : mem) {
+          const int32_t s0 = reqs[r].kv_length - (reqs[r].q_end - reqs[r].q_start);
+          if ((int64_t)(L + 1) * ps > s0) ok = false;
+        }
+        if (!ok) break;
+        const int32_t page = bt[(size_t)mem[0] * mb + L];
+        for (int32_t r : mem) {
+          if (bt[(size_t)r * mb + L] != page) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
+      }
+      if (L < 1) continue;
+      Sequence s;
+      s.bt_row = mem[0];
+      s.k_begin = 0;
+      s.k_end = L * ps;
+      s.members = mem;
+      s.shared = true;
+      seqs.push_back(s);
+      for (int32_t r : mem) own_begin[r] = L * ps;
+      ++n_groups;
+      cascade_keys += L * ps;
+    }
+  }
+  for (int32_t r : decode_reqs) {
+    Sequence s;
+    s.bt_row = r;
+    s.k_begin = own_begin[r];
+    s.k_end = reqs[r].kv_length;
+    s.members = {r};
+    s.shared = false;
+    seqs.push_back(s);
+  }
+
+  // ---- split-KV chunk size ---------------------------------------------
+  int64_t work = 0;  // key-visits summed over CTAs if nothing were split
+  for (const Sequence& s : seqs) {
+    int64_t rows = 0;
+    for (int32_t r : s.members) rows += (int64_t)(reqs[r].q_end - reqs[r].q_start) * g;
+    const int64_t groups = (rows + kRowsPerDecodeItem - 1) / kRowsPerDecodeItem;
+    work += (int64_t)(s.k_end - s.k_begin) * groups * Hkv;
+  }
+  int32_t chunk = o.kv_chunk;
+  if (chunk == 0) {
+    int64_t c = (work + target - 1) / std::max(1, target);
+    c = ((c + 63) / 64) * 64;
+    chunk = (int32_t)std::min<int64_t>(std::max<int64_t>(c, kMinChunk), 1 << 30);
+  }
+  auto n_chunks = [&](const Sequence& s) -> int32_t {
+    const int32_t len = s.k_end - s.k_begin;
+    return len <= 0 ? 0 : (len + chunk - 1) / chunk;
+  };
+
+  // ---- partial slots per output row ------------------------------------
+  // every output row of a split-KV request owns n_slots contiguous partial
+  // slots: first the chunks of its shared prefix (if any), then its own.
+  std::vector<int32_t> shared_chunks(n, 0), own_chunks(n, 0), slot_base(n, -1);
+  for (const Sequence& s : seqs)
+    for (int32_t r : s.members) {
+      if (s.shared)
+        shared_chunks[r] = n_chunks(s);
+      else
+        own_chunks[r] = n_chunks(s);
+    }
+  int32_t n_partials = 0;
+  std::vector<CombineEntry> combine;
+  for (int32_t r : decode_reqs) {
+    const int32_t slots = shared_chunks[r] + own_chunks[r];
+    if (slots <= 1) continue;
+    slot_base[r] = n_partials;
+    const int32_t m = reqs[r].q_end - reqs[r].q_start;
+    for (int32_t i = 0; i < m; ++i)
+      for (int32_t h = 0; h < Hq; ++h) {
+        CombineEntry e;
+        e.q_index = reqs[r].q_start + i;
+        e.q_head = h;
+        e.slot_begin = n_partials;
+        e.n_slots = slots;
+        combine.push_back(e);
+        n_partials += slots;
+      }
+  }
+  auto slot_of = [&](int32_t r, int32_t i, int32_t hq, bool shared, int32_t c) -> int32_t {
+    if (slot_base[r] < 0) return -1;
+    const int32_t slots = shared_chunks[r] + own_chunks[r];
+    const int32_t idx = shared ? c : shared_chunks[r] + c;
+    return slot_base[r] + (i * Hq + hq) * slots + idx;
+  };
+
+  // ---- split-KV items and row descriptors -----------------------------
+  std::vector<DecodeItem> items;
+  std::vector<RowDesc> rows;
+  for (const Sequence& s : seqs) {
+    const int32_t nc = n_chunks(s);
+    for (int32_t h = 0; h < Hkv; ++h) {
+      // the rows of this KV head: members x new rows x the g query heads
+      struct R { int32_t r, i, hq; };
+      std::vector<R> rr;
+      for (int32_t r : s.members) {
+        const int32_t m = reqs[r].q_end - reqs[r].q_start;
+        for (int32_t i = 0; i < m; ++i)
+          for (int32_t j = 0; j < g; ++j) rr.push_back({r, i, h * g + j});
+      }
+      for (int32_t c = 0; c < nc; ++c) {
+        const int32_t kb = s.k_begin + c * chunk;
+        const int32_t ke = std::min(s.k_end, kb + chunk);
+        for (size_t p = 0; p < rr.size(); p += kRowsPerDecodeItem) {
+          DecodeItem it = {};
+          it.bt_row = s.bt_row;
+          it.kv_head = h;
+          it.k_begin = kb;
+          it.k_end = ke;
+          it.row_begin = (int32_t)rows.size();
+          it.n_rows = (int32_t)std::min<size_t>(kRowsPerDecodeItem, rr.size() - p);
+          for (int32_t k = 0; k < it.n_rows; ++k) {
+            const R& x = rr[p + k];
+            const mb_request_t& q = reqs[x.r];
+            const int32_t s0 = q.kv_length - (q.q_end - q.q_start);
+            RowDesc d;
+            d.q_index = q.q_start + x.i;
+            d.q_head = x.hq;
+            d.vis_end = s0 + x.i + 1;
+            d.dst = slot_of(x.r, x.i, x.hq, s.shared, c);
+            rows.push_back(d);
+          }
+          items.push_back(it);
+        }
+      }
+    }
+  }
+
+  // ---- prefill items, heaviest first -----------------------------------
+  std::vector<PrefillItem> pitems;
+  for (int32_t r : prefill_reqs) {
+    const mb_request_t& q = reqs[r];
+    const int32_t m = q.q_end - q.q_start, s0 = q.kv_length - m;
+    for (int32_t h = 0; h < Hq; ++h)
+      for (int32_t i0 = 0; i0 < m; i0 += kPrefillTileM) {
+        PrefillItem p;
+        p.req = r;
+        p.q_head = h;
+        p.q_row0 = q.q_start + i0;
+        p.n_rows = std::min(kPrefillTileM, m - i0);
+        p.s0 = s0;
+        p.i0 = i0;
+        p.kv_length = q.kv_length;
+        const int32_t last = std::min(q.kv_length, s0 + i0 + p.n_rows);
+        p.n_kv_tiles = (last + kPrefillTileN - 1) / kPrefillTileN;
+        pitems.push_back(p);
+      }
+  }
+  std::stable_sort(pitems.begin(), pitems.end(),
+                   [](const PrefillItem& a, const PrefillItem& b) {
+                     return a.n_kv_tiles > b.n_kv_tiles;
+                   });
+
+  // ---- workspace layout + host image -----------------------------------
+  PlanDevice& d = plan->dev;
+  d = PlanDevice{};
+  d.n_decode_items = (int32_t)items.size();
+  d.n_decode_rows = (int32_t)rows.size();
+  d.n_prefill_items = (int32_t)pitems.size();
+  d.n_combine = (int32_t)combine.size();
+  d.n_partials = n_partials;
+  d.n_q_heads = Hq;
+  d.n_kv_heads = Hkv;
+  d.head_dim = D;
+  d.page_size = ps;
+  d.num_pages = cfg->num_pages;
+  d.max_blocks = mb;
+  d.total_q = total_q;
+  d.scale = cfg->scale > 0.f ? cfg->scale : 1.0f / sqrtf((float)D);
+  size_t off = kStatusBytes;
+  d.off_decode_items = off;
+  off = align256(off + items.size() * sizeof(DecodeItem));
+  d.off_rows = off;
+  off = align256(off + rows.size() * sizeof(RowDesc));
+  d.off_prefill_items = off;
+  off = align256(off + pitems.size() * sizeof(PrefillItem));
+  d.off_combine = off;
+  off = align256(off + combine.size() * sizeof(CombineEntry));
+  d.metadata_bytes = off;
+  d.off_part_lse = off;
+  off = align256(off + (size_t)n_partials * sizeof(float));
+  d.off_part_o = off;
+  off = align256(off + (size_t)n_partials * D * sizeof(float));
+  d.workspace_bytes = off;
+
+  plan->host_image.assign(d.metadata_bytes, 0);
+  uint8_t* img = plan->host_image.data();
+  if (!items.empty())
+    memcpy(img + d.off_decode_items, items.data(), items.size() * sizeof(DecodeItem));
+  if (!rows.empty()) memcpy(img + d.off_rows, rows.data(), rows.size() * sizeof(RowDesc));
+  if (!pitems.empty())
+    memcpy(img + d.off_prefill_items, pitems.data(), pitems.size() * sizeof(PrefillItem));
+  if (!combine.empty())
+    memcpy(img + d.off_combine, combine.data(), combine.size() * sizeof(CombineEntry));
+
+  mb_plan_info_t& info = plan->info;
+  info = mb_plan_info_t{};
+  info.n_decode_items = d.n_decode_items;
+  info.n_decode_rows = d.n_decode_rows;
+  info.n_prefill_items = d.n_prefill_items;
+  info.n_combine = d.n_combine;
+  info.n_partials = n_partials;
+  info.n_cascade_groups = n_groups;
+  info.cascade_keys = cascade_keys;
+  info.kv_chunk = chunk;
+  info.total_q = total_q;
+  info.n_launches = (d.n_decode_items > 0) + (d.n_prefill_items > 0) + (d.n_combine > 0);
+  info.workspace_bytes = d.workspace_bytes;
+  info.metadata_bytes = d.metadata_bytes;
+  return MB_OK;
+}
+
+// ---- pinned staging for the plan upload --------------------------------
+// A copy from pageable memory makes the host wait for the stream's earlier
+// work; the plan therefore uploads from page-locked buffers. Buffers are
+// recycled once the event recorded after their copy has completed, so no
+// call here blocks on the device.
+namespace {
+struct Staging {
+  int device;
+  void* ptr;
+  size_t cap;
+  cudaEvent_t done;
+  bool in_use;
+};
+std::mutex g_staging_mu;
+std::vector<Staging>* g_staging = new std::vector<Staging>();  // never freed: outlives exit
+}  // namespace
+
+int staging_acquire(int device, size_t bytes) {
+  std::lock_guard<std::mutex> lk(g_staging_mu);
+  for (size_t i = 0; i < g_staging->size(); ++i) {
+    Staging& b = (*g_staging)[i];
+    if (b.in_use || b.device != device || b.cap < bytes) continue;
+    if (cudaEventQuery(b.done) != cudaSuccess) continue;
+    b.in_use = true;
+    return (int)i;
+  }
+  Staging b;
+  b.device = device;
+  b.cap = std::max<size_t>(bytes, 64 * 1024);
+  if (cudaHostAlloc(&b.ptr, b.cap, cudaHostAllocDefault) != cudaSuccess) return -1;
+  if (cudaEventCreateWithFlags(&b.done, cudaEventDisableTiming) != cudaSuccess) {
+    cudaFreeHost(b.ptr);
+    return -1;
+  }
+  b.in_use = true;
+  g_staging->push_back(b);
+  return (int)g_staging->size() - 1;
+}
+
+void* staging_ptr(int idx) {
+  std::lock_guard<std::mutex> lk(g_staging_mu);
+  return (*g_staging)[idx].ptr;
+}
+
+cudaError_t staging_record(int idx, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_staging_mu);
+  return cudaEventRecord((*g_staging)[idx].done, s);
+}
+
+void staging_release(int idx) {
+  std::lock_guard<std::mutex> lk(g_staging_mu);
+  if (idx >= 0 && idx < (int)g_staging->size()) (*g_staging)[idx].in_use = false;
+}
+
+}  // namespace mb
+
+extern "C" {
+
+int32_t mb_abi_version(void) { return MB_ABI_VERSION; }
+
+const char* mb_status_string(mb_status_t s) {
+  switch (s) {
+    case MB_OK: return "ok";
+    case MB_ERR_INVALID_ARG: return "invalid argument";
+    case MB_ERR_SHAPE: return "inconsistent shapes, triples or block table";
+    case MB_ERR_UNSUPPORTED: return "unsupported head_dim / page_size / size";
+    case MB_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case MB_ERR_CUDA: return "CUDA runtime error";
+    case MB_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case MB_ERR_DEVICE_INDEX: return "device-side index out of range";
+  }
+  return "unknown status";
+}
+
+mb_status_t mb_slot_mapping(const mb_request_t* reqs, int32_t n_reqs,
+                            const int32_t* block_table_host,
+                            const mb_config_t* cfg, int32_t* slots_out,
+                            int32_t total_q) {
+  mb_status_t st = validate_config(cfg);
+  if (st != MB_OK) return st;
+  int32_t tq = 0;
+  st = validate_requests(reqs, n_reqs, block_table_host, cfg, &tq);
+  if (st != MB_OK) return st;
+  if (total_q < tq || total_q < 0) return MB_ERR_SHAPE;
+  if (total_q > 0 && !slots_out) return MB_ERR_INVALID_ARG;
+  const int ps = cfg->page_size, mb = cfg->max_blocks_per_req;
+  for (int32_t t = 0; t < total_q; ++t) slots_out[t] = -1;
+  for (int32_t r = 0; r < n_reqs; ++r) {
+    const mb_request_t& q = reqs[r];
+    const int32_t s0 = q.kv_length - (q.q_end - q.q_start);
+    for (int32_t t = q.q_start; t < q.q_end; ++t) {
+      const int32_t p = s0 + (t - q.q_start);
+      const int32_t page = block_table_host[(size_t)r * mb + p / ps];
+      slots_out[t] = page * ps + p % ps;
+    }
+  }
+  return MB_OK;
+}
+
+mb_status_t mb_attn_plan_ex(const mb_request_t* reqs, int32_t n_reqs,
+                            const int32_t* block_table_host,
+                            const mb_config_t* cfg,
+                            const mb_plan_options_t* opts, void* workspace,
+                            size_t* workspace_bytes, cudaStream_t stream,
+                            mb_plan_t** out_plan) {
+  if (!workspace_bytes) return MB_ERR_INVALID_ARG;
+  mb_plan* plan = new (std::nothrow) mb_plan();
+  if (!plan) return MB_ERR_INVALID_ARG;
+  mb_status_t st = mb::build_plan(reqs, n_reqs, block_table_host, cfg, opts, plan);
+  if (st != MB_OK) {
+    delete plan;
+    return st;
+  }
+  if (!workspace) {  // size query
+    *workspace_bytes = plan->dev.workspace_bytes;
+    delete plan;
+    return MB_OK;
+  }
+  if (!out_plan) {
+    delete plan;
+    return MB_ERR_INVALID_ARG;
+  }
+  if (*workspace_bytes < plan->dev.workspace_bytes ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255) != 0) {
+    delete plan;
+    return MB_ERR_WORKSPACE;
+  }
+  plan->workspace = workspace;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) {
+    delete plan;
+    return MB_ERR_CUDA;
+  }
+  const size_t nb = plan->dev.metadata_bytes;
+  plan->staging = mb::staging_acquire(device, nb);
+  if (plan->staging < 0) {
+    delete plan;
+    return MB_ERR_CUDA;
+  }
+  memcpy(mb::staging_ptr(plan->staging), plan->host_image.data(), nb);
+  cudaError_t e = cudaMemcpyAsync(workspace, mb::staging_ptr(plan->staging), nb,
+                                  cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = mb::staging_record(plan->staging, stream);
+  if (e != cudaSuccess) {
+    mb::staging_release(plan->staging);
+    delete plan;
+    return MB_ERR_CUDA;
+  }
+  *out_plan = plan;
+  return MB_OK;
+}
+
+mb_status_t mb_attn_plan(const mb_request_t* reqs, int32_t n_reqs,
+                         const int32_t* block_table_host, const mb_config_t* cfg,
+                         void* workspace, size_t* workspace_bytes,
+                         cudaStream_t stream, mb_plan_t** out_plan) {
+  return mb_attn_plan_ex(reqs, n_reqs, block_table_host, cfg, nullptr, workspace,
+                         workspace_bytes, stream, out_plan);
+}
+
+mb_status_t mb_attn_plan_host(const mb_request_t* reqs, int32_t n_reqs,
+                              const int32_t* block_table_host, const mb_config_t* cfg,
+                              const mb_plan_options_t* opts, mb_plan_t** out_plan) {
+  if (!out_plan) return MB_ERR_INVALID_ARG;
+  mb_plan* plan = new (std::nothrow) mb_plan();
+  if (!plan) return MB_ERR_INVALID_ARG;
+  mb_status_t st = mb::build_plan(reqs, n_reqs, block_table_host, cfg, opts, plan);
+  if (st != MB_OK) {
+    delete plan;
+    return st;
+  }
+  *out_plan = plan;
+  return MB_OK;
+}
+
+mb_status_t mb_plan_export_metadata(const mb_plan_t* plan, void* dst, size_t dst_bytes) {
+  if (!plan || !dst || dst_bytes < plan->host_image.size()) return MB_ERR_INVALID_ARG;
+  memcpy(dst, plan->host_image.data(), plan->host_image.size());
+  return MB_OK;
+}
+
+mb_status_t mb_plan_layout(const mb_plan_t* plan, size_t* out6) {
+  if (!plan || !out6) return MB_ERR_INVALID_ARG;
+  out6[0] = plan->dev.off_decode_items;
+  out6[1] = plan->dev.off_rows;
+  out6[2] = plan->dev.off_prefill_items;
+  out6[3] = plan->dev.off_combine;
+  out6[4] = plan->dev.off_part_lse;
+  out6[5] = plan->dev.off_part_o;
+  return MB_OK;
+}
+
+mb_status_t mb_plan_info(const mb_plan_t* plan, mb_plan_info_t* info) {
+  if (!plan || !info) return MB_ERR_INVALID_ARG;
+  *info = plan->info;
+  return MB_OK;
+}
+
+mb_status_t mb_attn_destroy(mb_plan_t* plan) {
+  if (plan && plan->staging >= 0) mb::staging_release(plan->staging);
+  delete plan;
+  return MB_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,239 @@
+/*
+ * mb.h -- C ABI of the mixed-batch paged attention library (one GB300, sm_103a).
+ *
+ * The library computes the attention step of one continuous-batching
+ * iteration (one layer): a ragged batch of requests, each described by the
+ * triple (q_start, q_end, kv_length), whose new query rows attend to their
+ * own paged K/V cache.
+ *
+ *   - Per-request triple, kv_length counted after this iteration's append:
+ *     "ORCA and chunked prefill", section 2.
+ *   - Mask: the first S0 = kv_length - q_rows key columns are visible to every
+ *     new row; over the last q_rows columns only the strict upper triangle is
+ *     masked (diagonal kept): "How To Scale Your Model notes (7-8)", section 2;
+ *     the same two blocks in "ORCA and chunked prefill", section 4.
+ *   - Paged K/V through a per-request block table, pages shareable between
+ *     requests: "How To Scale Your Model notes (7-8)", section 3 (paging);
+ *     slot mapping ("out_cache_loc") and block tables built by the host:
+ *     "GLM-5.3 e2e token ledger", stage 4.
+ *   - GQA: g = n_q_heads / n_kv_heads query heads share KV head h / g
+ *     (contiguous grouping): "How To Scale Your Model notes (7-8)", section 3.
+ *   - Shared prefix read once for all requests that share it, each request
+ *     keeping its own softmax state: "How To Scale Your Model notes (7-8)",
+ *     section 3 (stored once is not read once).
+ *
+ * Layouts (all row-major, contiguous, bf16 = IEEE bfloat16 bit patterns):
+ *   q, out      [total_q, n_q_heads, head_dim]            bf16
+ *   lse         [total_q, n_q_heads]                      fp32 (natural log)
+ *   k_new/v_new [T, n_kv_heads, head_dim]                 bf16
+ *   k_cache,
+ *   v_cache     [num_pages, n_kv_heads, page_size, head_dim] bf16
+ *               (one page of one KV head is one contiguous
+ *                page_size * head_dim * 2 byte tile)
+ *   block_table [n_reqs, max_blocks_per_req]               int32 page ids;
+ *               entry b of request r holds logical positions
+ *               [b * page_size, (b + 1) * page_size)
+ *   slot        page * page_size + position % page_size    int32
+ *
+ * Ownership: the caller owns every device buffer (caches, q, out, lse,
+ * block tables, slot mappings, the workspace) and the stream. The library
+ * never allocates device memory and never synchronises the device; a plan
+ * owns only host memory. Calls enqueue work on the caller's stream.
+ *
+ * Errors: host-detectable errors are returned as mb_status_t and nothing is
+ * enqueued. Device-detected errors (a slot or page out of range, a bounded
+ * wait that ran out) are OR-ed as bit flags (1 << status) into a device
+ * int32 status word: the one passed to mb_kv_append, and for attention the
+ * first 4 bytes of the plan's workspace. The caller reads it after a sync.
+ */
+#ifndef MB_H
+#define MB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MB_ABI_VERSION 1
+
+typedef enum {
+  MB_OK = 0,
+  MB_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad option        */
+  MB_ERR_SHAPE = 2,        /* inconsistent triples / block table / config    */
+  MB_ERR_UNSUPPORTED = 3,  /* head_dim or page_size outside the built set    */
+  MB_ERR_WORKSPACE = 4,    /* workspace missing, too small or misaligned     */
+  MB_ERR_CUDA = 5,         /* a CUDA runtime call failed                     */
+  MB_ERR_TIMEOUT = 6,      /* device flag: a bounded wait in a kernel ran out */
+  MB_ERR_DEVICE_INDEX = 7  /* device flag: slot / page index out of range    */
+} mb_status_t;
+
+/* One request of the iteration ("ORCA and chunked prefill", section 2).
+ * q_rows = q_end - q_start new rows at rows [q_start, q_end) of q / out;
+ * kv_length = whole context including this iteration's q_rows rows, so the
+ * new rows occupy logical positions [kv_length - q_rows, kv_length).
+ * q_rows = 0 is allowed (no output). */
+typedef struct {
+  int32_t q_start;
+  int32_t q_end;
+  int32_t kv_length;
+} mb_request_t;
+
+/* Problem configuration shared by every call of one layer. */
+typedef struct {
+  int32_t n_q_heads;           /* Hq, multiple of n_kv_heads                  */
+  int32_t n_kv_heads;          /* Hkv                                          */
+  int32_t head_dim;            /* D: 64 or 128                                 */
+  int32_t page_size;           /* tokens per page: 16, 32, 64 or 128           */
+  int32_t num_pages;           /* pages in each of k_cache / v_cache           */
+  int32_t max_blocks_per_req;  /* columns of the block table                   */
+  float scale;                 /* softmax scale; 0 -> 1/sqrt(head_dim)         */
+} mb_config_t;
+
+/* Planner knobs (mb_attn_plan_ex). Zero-initialised = defaults. */
+typedef struct {
+  int32_t prefill_min_rows;  /* requests with q_rows >= this run the tensor-core
+                                prefill kernel; 0 -> default (16);
+                                < 0 -> never (everything on split-KV)        */
+  int32_t kv_chunk;          /* split-KV chunk in keys (multiple of 64);
+                                0 -> chosen from the batch                   */
+  int32_t disable_cascade;   /* 1 -> no shared-prefix grouping               */
+  int32_t target_ctas;       /* split-KV work items to aim for; 0 -> auto     */
+} mb_plan_options_t;
+
+/* Plan summary (mb_plan_info). */
+typedef struct {
+  int32_t n_decode_items;    /* CTAs of the split-KV kernel                   */
+  int32_t n_decode_rows;     /* row descriptors                               */
+  int32_t n_prefill_items;   /* CTAs of the prefill kernel                    */
+  int32_t n_combine;         /* output rows merged by the combine kernel      */
+  int32_t n_partials;        /* partial (O, LSE) slots                        */
+  int32_t n_cascade_groups;  /* shared-prefix groups                          */
+  int32_t cascade_keys;      /* keys read once per group (sum over groups)    */
+  int32_t kv_chunk;          /* split-KV chunk actually used                  */
+  int32_t total_q;           /* max q_end                                     */
+  int32_t n_launches;        /* kernels one mb_attn_forward launches          */
+  size_t workspace_bytes;
+  size_t metadata_bytes;     /* bytes uploaded host->device by the plan       */
+} mb_plan_info_t;
+
+typedef struct mb_plan mb_plan_t;
+
+/* Stages timed by mb_attn_forward_timed, in launch order. */
+#define MB_STAGE_DECODE 0
+#define MB_STAGE_COMBINE 1
+#define MB_STAGE_PREFILL 2
+#define MB_NUM_STAGES 3
+
+int32_t mb_abi_version(void);
+const char* mb_status_string(mb_status_t s);
+
+/* Host helper: the slot ("out_cache_loc") of every new row, i.e. where
+ * mb_kv_append writes it ("GLM-5.3 e2e token ledger", stage 4).
+ * New row t of request r sits at logical position p = kv_length - q_rows +
+ * (t - q_start), slot = block_table[r][p / page_size] * page_size +
+ * p % page_size. slots_out (host, total_q entries) receives -1 for rows no
+ * request covers. block_table_host is [n_reqs, cfg->max_blocks_per_req].
+ * Errors: MB_ERR_INVALID_ARG, MB_ERR_SHAPE (same checks as mb_attn_plan). */
+mb_status_t mb_slot_mapping(const mb_request_t* reqs, int32_t n_reqs,
+                            const int32_t* block_table_host,
+                            const mb_config_t* cfg, int32_t* slots_out,
+                            int32_t total_q);
+
+/* KV append: scatter this iteration's K/V rows into their pages
+ * ("ORCA and chunked prefill", section 4: append K, V to the cache before
+ * the attention reads it). For t in [0, T): slot = slot_mapping[t];
+ * slot < 0 skips the row (padding); otherwise every KV head h gets
+ *   k_cache[slot / ps][h][slot % ps][:] = k_new[t][h][:]  (same for V),
+ * a bit-exact copy. k_new/v_new [T, Hkv, D] contiguous bf16 (device);
+ * slot_mapping int32 [T] (device). Pages written here must not be shared
+ * with another request (the caller's contract). A slot >= num_pages*ps is
+ * skipped and sets bit (1 << MB_ERR_DEVICE_INDEX) in *status_dev
+ * (nullable device int32). T = 0 enqueues nothing. Asynchronous on stream. */
+mb_status_t mb_kv_append(void* k_cache, void* v_cache, const void* k_new,
+                         const void* v_new, const int32_t* slot_mapping,
+                         int32_t T, const mb_config_t* cfg, int32_t* status_dev,
+                         cudaStream_t stream);
+
+/* Plan one iteration. Host inputs: reqs[n_reqs] and block_table_host
+ * [n_reqs, max_blocks_per_req]. Validates: config (Hq % Hkv == 0, head_dim,
+ * page_size), 0 <= q_start <= q_end, q_rows <= kv_length, disjoint q
+ * ranges, ceil(kv_length / page_size) <= max_blocks_per_req, every used
+ * block id in [0, num_pages). Classifies requests (tensor-core prefill vs
+ * split-KV), groups requests whose leading cached pages are the same
+ * physical pages (shared-prefix cascade), splits long key ranges into
+ * split-KV chunks and lays out the workspace.
+ * workspace == NULL: size query; *workspace_bytes receives the size and
+ * *out_plan is untouched. Otherwise workspace (device, 256-byte aligned,
+ * >= that size, owned by the caller, kept alive and unmodified while the
+ * plan is used) receives the work lists with one host->device copy on
+ * stream, and *out_plan a new plan (free with mb_attn_destroy). The plan
+ * may be reused by any number of mb_attn_forward calls (e.g. every layer
+ * of the iteration). */
+mb_status_t mb_attn_plan(const mb_request_t* reqs, int32_t n_reqs,
+                         const int32_t* block_table_host, const mb_config_t* cfg,
+                         void* workspace, size_t* workspace_bytes,
+                         cudaStream_t stream, mb_plan_t** out_plan);
+
+/* mb_attn_plan with explicit planner knobs (opts may be NULL). */
+mb_status_t mb_attn_plan_ex(const mb_request_t* reqs, int32_t n_reqs,
+                            const int32_t* block_table_host,
+                            const mb_config_t* cfg,
+                            const mb_plan_options_t* opts, void* workspace,
+                            size_t* workspace_bytes, cudaStream_t stream,
+                            mb_plan_t** out_plan);
+
+/* Attention of every planned request. q [total_q, Hq, D] bf16, caches as
+ * above (already holding this iteration's rows), block_table_dev: device
+ * copy of the planned block table, out [total_q, Hq, D] bf16 (rows no
+ * request covers are not written), lse [total_q, Hq] fp32 natural-log
+ * log-sum-exp of the scaled visible scores (nullable). No device->host
+ * traffic and no allocation: the launch sequence can be captured in a CUDA
+ * graph. Device-detected errors go to the workspace status word. */
+mb_status_t mb_attn_forward(const mb_plan_t* plan, const void* q,
+                            const void* k_cache, const void* v_cache,
+                            const int32_t* block_table_dev, void* out,
+                            float* lse, cudaStream_t stream);
+
+/* mb_attn_forward that also records events[2*s] / events[2*s+1] on stream
+ * around stage s (MB_STAGE_*) when that stage launches. events: array of
+ * 2 * MB_NUM_STAGES created events (entries may be NULL). */
+mb_status_t mb_attn_forward_timed(const mb_plan_t* plan, const void* q,
+                                  const void* k_cache, const void* v_cache,
+                                  const int32_t* block_table_dev, void* out,
+                                  float* lse, cudaStream_t stream,
+                                  cudaEvent_t* events);
+
+/* Host-only planning for inspection: builds the plan (same validation and
+ * work lists as mb_attn_plan_ex) without a workspace and without any CUDA
+ * call. Such a plan cannot be passed to mb_attn_forward (MB_ERR_INVALID_ARG);
+ * it serves mb_plan_info / mb_plan_export_metadata. */
+mb_status_t mb_attn_plan_host(const mb_request_t* reqs, int32_t n_reqs,
+                              const int32_t* block_table_host, const mb_config_t* cfg,
+                              const mb_plan_options_t* opts, mb_plan_t** out_plan);
+
+/* Copy the plan's metadata image (the bytes mb_attn_plan uploads to the
+ * start of the workspace; info.metadata_bytes long) into host memory dst of
+ * dst_bytes. Its layout: int32 status word at 0, then the work lists at the
+ * offsets given by mb_plan_layout. */
+mb_status_t mb_plan_export_metadata(const mb_plan_t* plan, void* dst, size_t dst_bytes);
+
+/* Byte offsets of the workspace regions: out[0..5] = decode items, row
+ * descriptors, prefill items, combine entries, partial LSEs, partial outputs. */
+mb_status_t mb_plan_layout(const mb_plan_t* plan, size_t* out6);
+
+/* Summary of a plan (host only). */
+mb_status_t mb_plan_info(const mb_plan_t* plan, mb_plan_info_t* info);
+
+/* Release a plan's host memory. NULL is accepted. The workspace stays the
+ * caller's. */
+mb_status_t mb_attn_destroy(mb_plan_t* plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MB_H */

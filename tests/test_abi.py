@@ -1,0 +1,234 @@
+"""C ABI and host planner tests (no GPU: only host-side entry points run).
+
+* the library loads and exports every function ``include/mb.h`` declares;
+* argument validation returns the documented status codes;
+* ``mb_slot_mapping`` places rows where the oracle's addressing does;
+* the planner's work lists cover every visible (row, head, key) exactly once,
+  send each row's partials to one combine entry, and group shared prefixes.
+"""
+
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+from continuous_batching_paged_varlen_gb300 import binding as B
+from continuous_batching_paged_varlen_gb300 import build as build_mod
+from continuous_batching_paged_varlen_gb300 import workloads as W
+from oracle import attention as OA
+from tests.conftest import ROOT, read_int_table
+
+HEADER = os.path.join(ROOT, "include", "mb.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_mod.build()
+    return B.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mb_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert {"mb_kv_append", "mb_attn_plan", "mb_attn_forward", "mb_attn_destroy"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+    assert L.mb_abi_version() == 1
+    assert L.mb_status_string(0) == b"ok"
+
+
+def cfg_for(w):
+    s = w.spec
+    return B.config(s.n_q_heads, s.n_kv_heads, s.head_dim, s.page_size, w.num_pages,
+                    w.block_table.shape[1], s.scale or 0.0)
+
+
+def test_slot_mapping_hand_worked_fixture(L):
+    """tests/golden/append_tiny_ps16.txt, worked by hand from the addressing rule."""
+    rows = read_int_table("append_tiny_ps16.txt")
+    cfg = B.config(1, 1, 64, 16, 8, 3)
+    bt = np.array([[5, 2, -1], [0, 7, 4]], dtype=np.int32)
+    slots = B.slot_mapping([(0, 3, 18), (3, 4, 33)], bt, cfg, 4)
+    assert slots.tolist() == [flat for _, _, _, flat in rows]
+    for t, page, slot, flat in rows:
+        assert flat == page * 16 + slot
+
+
+@pytest.mark.parametrize("name", ["tiny_mixed", "llama2_7b_orca_iteration", "decode_heavy_gqa4",
+                                  "shared_prefix_decode"])
+def test_slot_mapping_matches_oracle_addressing(L, name):
+    w = W.make_workload(name, with_values=False)
+    cfg = cfg_for(w)
+    slots = B.slot_mapping(w.requests, w.block_table, cfg, w.total_q)
+    ps = w.spec.page_size
+    for r, (qs, qe, kv) in enumerate(w.requests.tolist()):
+        s0 = kv - (qe - qs)
+        for t in range(qs, qe):
+            page, slot = OA.logical_position_location(w.block_table[r], s0 + t - qs, ps)
+            assert slots[t] == page * ps + slot
+    assert len(set(slots.tolist())) == len(slots)  # no two new rows share a slot
+
+
+def _plan_status(reqs, bt, cfg, opts=None):
+    try:
+        B.HostPlan(reqs, bt, cfg, opts)
+        return 0
+    except B.MBError as e:
+        return e.status
+
+
+def test_validation_errors(L):
+    bt = np.array([[0, 1], [2, 3]], dtype=np.int32)
+    good = B.config(4, 2, 64, 16, 4, 2)
+    ok = [(0, 2, 20), (2, 3, 17)]
+    assert _plan_status(ok, bt, good) == 0
+    assert _plan_status([(0, 2, 1), (2, 3, 17)], bt, good) == 2        # q_rows > kv_length
+    assert _plan_status([(0, 2, 20), (1, 3, 17)], bt, good) == 2       # overlapping q ranges
+    assert _plan_status([(0, 2, 40), (2, 3, 17)], bt, good) == 2       # more blocks than columns
+    bad_bt = bt.copy()
+    bad_bt[1, 1] = 4
+    assert _plan_status(ok, bad_bt, good) == 2                         # page id out of the pool
+    assert _plan_status([(3, 2, 20)], bt[:1], good) == 2               # q_end < q_start
+    assert _plan_status(ok, bt, B.config(4, 3, 64, 16, 4, 2)) == 2     # Hq % Hkv
+    assert _plan_status(ok, bt, B.config(4, 2, 96, 16, 4, 2)) == 3     # head_dim
+    assert _plan_status(ok, bt, B.config(4, 2, 64, 24, 4, 2)) == 3     # page size
+    assert _plan_status(ok, bt, good, B.options(kv_chunk=100)) == 1    # chunk not /64
+    # q_rows = 0 requests are accepted and ignored (their table entries unused)
+    assert _plan_status([(0, 0, 0), (0, 1, 17)], np.array([[-1, -1], [2, 3]], np.int32), good) == 0
+    # empty batch
+    hp = B.HostPlan(np.zeros((0, 3), np.int32), np.zeros((0, 2), np.int32), good)
+    assert hp.info.total_q == 0 and hp.info.n_launches == 0
+    # slot mapping rejects a total_q smaller than the rows
+    with pytest.raises(B.MBError):
+        B.slot_mapping(ok, bt, good, 2)
+
+
+DECODE_ITEM = np.dtype([("bt_row", "<i4"), ("kv_head", "<i4"), ("k_begin", "<i4"),
+                        ("k_end", "<i4"), ("row_begin", "<i4"), ("n_rows", "<i4"),
+                        ("pad0", "<i4"), ("pad1", "<i4")])
+ROW = np.dtype([("q_index", "<i4"), ("q_head", "<i4"), ("vis_end", "<i4"), ("dst", "<i4")])
+PREFILL_ITEM = np.dtype([("req", "<i4"), ("q_head", "<i4"), ("q_row0", "<i4"),
+                         ("n_rows", "<i4"), ("s0", "<i4"), ("i0", "<i4"),
+                         ("kv_length", "<i4"), ("n_kv_tiles", "<i4")])
+COMBINE = np.dtype([("q_index", "<i4"), ("q_head", "<i4"), ("slot_begin", "<i4"),
+                    ("n_slots", "<i4")])
+
+
+def decode_plan(hp):
+    inf = hp.info
+    meta = np.frombuffer(hp.metadata(), dtype=np.uint8)
+    off = hp.layout()
+
+    def arr(o, dt, n):
+        return np.frombuffer(meta[o:o + n * dt.itemsize].tobytes(), dtype=dt)
+
+    assert np.all(meta[:4] == 0)  # status word starts cleared
+    return (arr(off[0], DECODE_ITEM, inf.n_decode_items), arr(off[1], ROW, inf.n_decode_rows),
+            arr(off[2], PREFILL_ITEM, inf.n_prefill_items), arr(off[3], COMBINE, inf.n_combine))
+
+
+def check_coverage(w, opts=None):
+    cfg = cfg_for(w)
+    hp = B.HostPlan(w.requests, w.block_table, cfg, opts)
+    items, rows, pitems, comb = decode_plan(hp)
+    inf = hp.info
+    s = w.spec
+    g = s.n_q_heads // s.n_kv_heads
+    ps = s.page_size
+    covered = {}     # (q_index, q_head) -> list of (k_begin, k_end, slot)
+    for it in items:
+        assert 1 <= it["n_rows"] <= 8
+        assert 0 <= it["k_begin"] < it["k_end"]
+        for rw in rows[it["row_begin"]:it["row_begin"] + it["n_rows"]]:
+            assert rw["q_head"] // g == it["kv_head"]          # one KV head per CTA
+            covered.setdefault((int(rw["q_index"]), int(rw["q_head"])), []).append(
+                (int(it["k_begin"]), int(it["k_end"]), int(rw["dst"]), int(rw["vis_end"]),
+                 int(it["bt_row"])))
+    pcover = {}
+    for p in pitems:
+        assert 1 <= p["n_rows"] <= 128
+        for i in range(p["n_rows"]):
+            key = (int(p["q_row0"]) + i, int(p["q_head"]))
+            assert key not in pcover
+            pcover[key] = p
+    slot_writes = {}
+    comb_by_row = {(int(c["q_index"]), int(c["q_head"])): c for c in comb}
+    assert len(comb_by_row) == len(comb)
+    for r, (qs, qe, kv) in enumerate(w.requests.tolist()):
+        m = qe - qs
+        s0 = kv - m
+        for i in range(m):
+            for h in range(s.n_q_heads):
+                key = (qs + i, h)
+                if key in pcover:
+                    p = pcover[key]
+                    assert key not in covered
+                    assert p["s0"] == s0 and p["kv_length"] == kv and p["i0"] + (qs + i - p["q_row0"]) == i
+                    last = min(kv, s0 + p["i0"] + p["n_rows"])
+                    assert p["n_kv_tiles"] == math.ceil(last / 128)
+                    # every visible key of the row lies in a visited tile
+                    assert p["n_kv_tiles"] * 128 >= s0 + i + 1
+                    continue
+                segs = sorted(covered[key])
+                # the key ranges tile [0, kv) exactly once
+                assert segs[0][0] == 0 and segs[-1][1] == kv
+                for a, b in zip(segs, segs[1:]):
+                    assert a[1] == b[0]
+                for kb, ke, dst, vis, btr in segs:
+                    assert vis == s0 + i + 1
+                    # the addressing row is this request's or shares its pages there
+                    nb0, nb1 = kb // ps, (ke - 1) // ps
+                    assert np.array_equal(w.block_table[btr, nb0:nb1 + 1],
+                                          w.block_table[r, nb0:nb1 + 1])
+                if len(segs) == 1:
+                    assert segs[0][2] < 0 and key not in comb_by_row
+                else:
+                    c = comb_by_row[key]
+                    assert c["n_slots"] == len(segs)
+                    assert sorted(sg[2] for sg in segs) == list(
+                        range(c["slot_begin"], c["slot_begin"] + c["n_slots"]))
+                    for sg in segs:
+                        assert sg[2] not in slot_writes
+                        slot_writes[sg[2]] = key
+    assert len(slot_writes) == inf.n_partials
+    return hp, inf
+
+
+@pytest.mark.parametrize("name", W.ORDER)
+def test_planner_coverage_default(L, name):
+    w = W.make_workload(name, with_values=False)
+    hp, inf = check_coverage(w)
+    if name == "shared_prefix_decode":
+        assert inf.n_cascade_groups == 1 and inf.cascade_keys == 4096
+    else:
+        assert inf.n_cascade_groups == 0
+    if name in ("llama2_7b_orca_iteration", "chunked_prefill_mix", "tiny_mixed"):
+        assert inf.n_prefill_items > 0
+
+
+@pytest.mark.parametrize("name", ["tiny_mixed", "shared_prefix_decode", "llama2_7b_orca_iteration"])
+@pytest.mark.parametrize("opts", [dict(prefill_min_rows=-1), dict(kv_chunk=64),
+                                  dict(kv_chunk=128, disable_cascade=1),
+                                  dict(prefill_min_rows=1, kv_chunk=256)])
+def test_planner_coverage_options(L, name, opts):
+    w = W.make_workload(name, with_values=False)
+    check_coverage(w, B.options(**opts))
+
+
+def test_prefill_tiles_skip_masked_tiles(L):
+    # one 4096-row prefill: tile t of 128 rows visits exactly t + 1 KV tiles
+    w = W.make_workload("llama2_7b_orca_iteration", with_values=False)
+    hp = B.HostPlan(w.requests, w.block_table, cfg_for(w))
+    _, _, pitems, _ = decode_plan(hp)
+    a = pitems[pitems["req"] == 0]
+    assert len(a) == 32 * 32
+    assert sorted(set((a["i0"] // 128 + 1 - a["n_kv_tiles"]).tolist())) == [0]
+    # heaviest first
+    assert np.all(np.diff(pitems["n_kv_tiles"]) <= 0)

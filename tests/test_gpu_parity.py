@@ -1,0 +1,186 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Caches are filled with NaN before the appends, so a kernel that reads an
+unwritten slot (or lets one reach the output through a zero weight) fails.
+Cache writes must be bit-exact; outputs and LSEs within atol = rtol = 2e-2.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from continuous_batching_paged_varlen_gb300 import binding as B
+from continuous_batching_paged_varlen_gb300 import workloads as W
+from oracle import attention as OA
+from tests.gpu_harness import (TOL, assert_request_close, cfg_of, custom_workload, fill_cache,
+                               run_forward)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from continuous_batching_paged_varlen_gb300 import build
+    build.build()
+    B.lib()
+
+
+# ------------------------------------------------------------------ append
+
+def oracle_cache_bits(w):
+    s = w.spec
+    kc = np.full((w.num_pages, s.n_kv_heads, s.page_size, s.head_dim), 0x7FC0, np.uint16)
+    vc = kc.copy()
+    as_bits = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)  # noqa: E731
+    OA.append_scatter(kc, vc, as_bits(w.k_hist), as_bits(w.v_hist), w.hist_requests,
+                      w.block_table, s.page_size)
+    OA.append_scatter(kc, vc, as_bits(w.k_new), as_bits(w.v_new), w.requests, w.block_table,
+                      s.page_size)
+    return kc, vc
+
+
+@pytest.mark.parametrize("name", ["tiny_mixed", "llama2_7b_orca_iteration",
+                                  "shared_prefix_decode"])
+def test_append_bit_exact(name):
+    w = W.make_workload(name)
+    kc, vc, _ = fill_cache(w)
+    ok, ov = oracle_cache_bits(w)
+    gk = kc.view(torch.int16).cpu().numpy().view(np.uint16)
+    gv = vc.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(gk, ok)
+    assert np.array_equal(gv, ov)
+
+
+def test_append_padding_and_bad_slot_flag():
+    w = W.make_workload("tiny_mixed")
+    cfg = cfg_of(w)
+    s = w.spec
+    kc = torch.zeros((w.num_pages, s.n_kv_heads, s.page_size, s.head_dim), dtype=torch.bfloat16,
+                     device="cuda")
+    vc = torch.zeros_like(kc)
+    kn = torch.randn(3, s.n_kv_heads, s.head_dim, device="cuda").to(torch.bfloat16)
+    vn = torch.randn(3, s.n_kv_heads, s.head_dim, device="cuda").to(torch.bfloat16)
+    slots = torch.tensor([5, -1, w.num_pages * s.page_size + 7], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.kv_append(kc, vc, kn, vn, slots, cfg, status)
+    torch.cuda.synchronize()
+    assert status.item() == 1 << B.MB_ERR_DEVICE_INDEX
+    assert torch.equal(kc[0, :, 5], kn[0]) and torch.equal(vc[0, :, 5], vn[0])
+    assert int((kc.float().abs().sum(dim=(1, 3)).cpu() != 0).sum()) == 1
+    # T = 0 enqueues nothing
+    B.kv_append(kc, vc, kn, vn, slots[:0], cfg, status)
+
+
+# --------------------------------------------------------------- attention
+
+OPTION_SETS = {
+    "default": None,
+    "all_split_kv": dict(prefill_min_rows=-1),
+    "all_prefill": dict(prefill_min_rows=1),
+    "chunk64": dict(kv_chunk=64),
+    "chunk256_nocascade": dict(kv_chunk=256, disable_cascade=1),
+}
+
+
+@pytest.mark.parametrize("opt", sorted(OPTION_SETS))
+def test_tiny_mixed_parity(opt):
+    w = W.make_workload("tiny_mixed")
+    kc, vc, cfg = fill_cache(w)
+    o = OPTION_SETS[opt]
+    out, lse, status, info = run_forward(w, kc, vc, cfg, B.options(**o) if o else None)
+    assert status == 0
+    for r in range(w.n_requests):
+        assert_request_close(w, out, lse, r)
+
+
+def test_llama_iteration_parity_sampled():
+    w = W.make_workload("llama2_7b_orca_iteration")
+    kc, vc, cfg = fill_cache(w)
+    out, lse, status, info = run_forward(w, kc, vc, cfg)
+    assert status == 0 and info["n_prefill_items"] == 32 * 32
+    assert torch.isfinite(out.float()).all()
+    # the 4096-row prefill: three heads in full (every tile, ragged-free)
+    assert_request_close(w, out, lse, 0, heads=[0, 13, 31])
+    # the two decodes: every head
+    assert_request_close(w, out, lse, 1)
+    assert_request_close(w, out, lse, 2)
+
+
+def test_decode_heavy_parity_sampled():
+    w = W.make_workload("decode_heavy_gqa4", device="cuda")
+    kc, vc, cfg = fill_cache(w)
+    out, lse, status, info = run_forward(w, kc, vc, cfg)
+    assert status == 0
+    assert torch.isfinite(out.float()).all()
+    rng = np.random.default_rng(0)
+    for r in sorted(rng.choice(w.n_requests, 12, replace=False).tolist()) + [0, w.n_requests - 1]:
+        assert_request_close(w, out, lse, r)
+
+
+def test_chunked_prefill_mix_parity_sampled():
+    w = W.make_workload("chunked_prefill_mix", device="cuda")
+    kc, vc, cfg = fill_cache(w)
+    out, lse, status, info = run_forward(w, kc, vc, cfg)
+    assert status == 0
+    assert torch.isfinite(out.float()).all()
+    # the 2048-row chunk at S0 = 30720: first, middle and last rows, two heads
+    for rows in [(0, 48), (1000, 1040), (2000, 2048)]:
+        assert_request_close(w, out, lse, 0, heads=[0, 29], rows=rows)
+    for r in [1, 17, 40, 64]:
+        assert_request_close(w, out, lse, r)
+
+
+@pytest.mark.parametrize("cascade", [True, False])
+def test_shared_prefix_parity(cascade):
+    w = W.make_workload("shared_prefix_decode", device="cuda")
+    kc, vc, cfg = fill_cache(w)
+    out, lse, status, info = run_forward(
+        w, kc, vc, cfg, None if cascade else B.options(disable_cascade=1))
+    assert status == 0
+    assert info["n_cascade_groups"] == (1 if cascade else 0)
+    for r in range(6):
+        assert_request_close(w, out, lse, r)
+
+
+EDGE_CASES = {
+    # name: (shapes, kwargs)
+    "q0_and_kv1": ([(0, 5), (1, 1), (3, 3), (1, 17)], {}),
+    "ragged_tiles_tail": ([(129, 300), (255, 255), (1, 77)], dict(n_q_heads=4, n_kv_heads=1)),
+    "page32_d128_g8": ([(40, 700), (1, 33), (2, 65)],
+                       dict(n_q_heads=16, n_kv_heads=2, head_dim=128, page_size=32)),
+    "page128_mha": ([(200, 1000), (1, 129), (16, 16)],
+                    dict(n_q_heads=2, n_kv_heads=2, head_dim=128, page_size=128)),
+    "page64_shared_pairs": ([(1, 600), (1, 700), (2, 650)],
+                            dict(n_q_heads=8, n_kv_heads=2, head_dim=128, page_size=64,
+                                 shared_prefix=512)),
+    "scale_override": ([(33, 90), (1, 50)], dict(scale=0.05)),
+}
+
+
+@pytest.mark.parametrize("case", sorted(EDGE_CASES))
+@pytest.mark.parametrize("opt", ["default", "all_split_kv", "all_prefill"])
+def test_edge_cases(case, opt):
+    shapes, kw = EDGE_CASES[case]
+    w = custom_workload(shapes, seed=sum(map(ord, case)), **kw)
+    kc, vc, cfg = fill_cache(w)
+    o = OPTION_SETS[opt]
+    out, lse, status, info = run_forward(w, kc, vc, cfg, B.options(**o) if o else None)
+    assert status == 0
+    for r in range(w.n_requests):
+        if w.requests[r, 1] > w.requests[r, 0]:
+            assert_request_close(w, out, lse, r)
+
+
+def test_deterministic_and_empty():
+    w = W.make_workload("tiny_mixed")
+    kc, vc, cfg = fill_cache(w)
+    a = run_forward(w, kc, vc, cfg)[0]
+    b = run_forward(w, kc, vc, cfg)[0]
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    empty = custom_workload([])
+    plan = B.Plan(empty.requests, np.zeros((0, 1), np.int32), cfg_of(empty))
+    assert plan.info.n_launches == 0
+    plan.forward(None, None, None, None, None)
+    plan.close()
