@@ -106,6 +106,8 @@ def lib():
     L.mb_plan_layout.argtypes = [_vp, ctypes.POINTER(ctypes.c_size_t)]
     L.mb_attn_destroy.restype = ctypes.c_int
     L.mb_attn_destroy.argtypes = [_vp]
+    L.mb_attn_forward_noalloc.restype = ctypes.c_int
+    L.mb_attn_forward_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
     _lib = L
     return L
 
@@ -200,6 +202,17 @@ class HostPlan:
             self.close()
         except Exception:
             pass
+
+
+def forward_noalloc(host_plan: "HostPlan", q, k_cache, v_cache, block_table_dev, out, lse=None,
+                    status=None, stream=None):
+    """``mb_attn_forward_noalloc``: run a host-only plan with the library's
+    static scratch array instead of a workspace (for callers that must not
+    allocate device memory; see include/mb.h)."""
+    check(lib().mb_attn_forward_noalloc(host_plan._h, _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(block_table_dev), _ptr(out), _ptr(lse),
+                                        _ptr(status), _stream_ptr(stream)),
+          "mb_attn_forward_noalloc")
 
 
 class Plan:

@@ -207,10 +207,10 @@ mb_status_t mb_attn_forward_timed(const mb_plan_t* plan, const void* q,
                                   float* lse, cudaStream_t stream,
                                   cudaEvent_t* events);
 
-/* Host-only planning for inspection: builds the plan (same validation and
- * work lists as mb_attn_plan_ex) without a workspace and without any CUDA
- * call. Such a plan cannot be passed to mb_attn_forward (MB_ERR_INVALID_ARG);
- * it serves mb_plan_info / mb_plan_export_metadata. */
+/* Host-only planning: builds the plan (same validation and work lists as
+ * mb_attn_plan_ex) without a workspace and without any CUDA call. Such a plan
+ * cannot be passed to mb_attn_forward (MB_ERR_INVALID_ARG); it serves
+ * mb_plan_info / mb_plan_export_metadata and mb_attn_forward_noalloc. */
 mb_status_t mb_attn_plan_host(const mb_request_t* reqs, int32_t n_reqs,
                               const int32_t* block_table_host, const mb_config_t* cfg,
                               const mb_plan_options_t* opts, mb_plan_t** out_plan);
@@ -227,6 +227,40 @@ mb_status_t mb_plan_layout(const mb_plan_t* plan, size_t* out6);
 
 /* Summary of a plan (host only). */
 mb_status_t mb_plan_info(const mb_plan_t* plan, mb_plan_info_t* info);
+
+/* Attention forward that allocates nothing (no counterpart on the pages:
+ * this is a convenience of the library, not part of the method).
+ *
+ * Who needs it: callers that must not allocate device memory themselves --
+ * for example code running under an external memory manager that owns every
+ * device allocation, a plug-in that is only handed pointers to its inputs and
+ * outputs, or a hot loop where a cudaMalloc (which can synchronise the whole
+ * device) is not acceptable. Such a caller builds its plan with
+ * mb_attn_plan_host (host memory only) and calls this instead of
+ * mb_attn_forward; no workspace is passed.
+ *
+ * The scratch the forward needs (the plan's work lists and the split-KV
+ * partial outputs) lives in one static device array inside the library,
+ * MB_NOALLOC_SCRATCH_BYTES long. Every GPU that loads the library holds that
+ * array until the process exits. A plan whose info.workspace_bytes exceeds
+ * the array is rejected with MB_ERR_WORKSPACE before anything is enqueued.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture. Each call
+ * copies the plan's work lists (from the plan's pageable host memory) into
+ * the array on `stream` -- this also clears the device status word -- then
+ * launches the same kernels as mb_attn_forward. Every call shares the one
+ * array and it keeps the last call's contents: calls whose work overlaps on
+ * the GPU (other streams, other host threads) race on it, so serialise them.
+ * status_dev (nullable, device int32) receives a copy of the call's device
+ * error flags (bits 1 << MB_ERR_TIMEOUT / MB_ERR_DEVICE_INDEX). Inputs,
+ * outputs and errors are otherwise as for mb_attn_forward. */
+#define MB_NOALLOC_SCRATCH_BYTES (8u << 20)
+mb_status_t mb_attn_forward_noalloc(const mb_plan_t* plan, const void* q,
+                                    const void* k_cache, const void* v_cache,
+                                    const int32_t* block_table_dev, void* out,
+                                    float* lse, int32_t* status_dev,
+                                    cudaStream_t stream);
 
 /* Release a plan's host memory. NULL is accepted. The workspace stays the
  * caller's. */
