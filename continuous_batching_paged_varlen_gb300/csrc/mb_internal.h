@@ -21,8 +21,9 @@ namespace mb {
 
 constexpr int kStatusBytes = 256;
 constexpr int kRowsPerDecodeItem = 8;   // query rows one split-KV CTA owns
-constexpr int kPrefillTileM = 128;      // query rows per prefill CTA
+constexpr int kPrefillTileM = 128;      // query rows per prefill tile (one TMEM accumulator)
 constexpr int kPrefillTileN = 128;      // keys per prefill KV tile
+constexpr int kPrefillCtaRows = 256;    // query rows per prefill CTA (two tiles)
 
 // One CTA of the split-KV kernel: query rows (all of one KV head) against
 // the key range [k_begin, k_end) of one block-table row.
@@ -43,8 +44,8 @@ struct RowDesc {
   int32_t dst;      // >= 0: partial slot; < 0: final row, write out / lse
 };
 
-// One CTA of the prefill kernel: up to kPrefillTileM consecutive new rows of
-// one request and one query head, against keys [0, n_kv_tiles * TileN).
+// One CTA of the prefill kernel: up to kPrefillCtaRows consecutive new rows
+// of one request and one query head, against keys [0, n_kv_tiles * TileN).
 struct PrefillItem {
   int32_t req;         // block-table row
   int32_t q_head;

@@ -284,12 +284,12 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
     const mb_request_t& q = reqs[r];
     const int32_t m = q.q_end - q.q_start, s0 = q.kv_length - m;
     for (int32_t h = 0; h < Hq; ++h)
-      for (int32_t i0 = 0; i0 < m; i0 += kPrefillTileM) {
+      for (int32_t i0 = 0; i0 < m; i0 += kPrefillCtaRows) {
         PrefillItem p;
         p.req = r;
         p.q_head = h;
         p.q_row0 = q.q_start + i0;
-        p.n_rows = std::min(kPrefillTileM, m - i0);
+        p.n_rows = std::min(kPrefillCtaRows, m - i0);
         p.s0 = s0;
         p.i0 = i0;
         p.kv_length = q.kv_length;

@@ -1,30 +1,37 @@
 // Prefill / chunk attention on the 5th-generation tensor cores (tcgen05).
 //
-// One CTA owns 128 consecutive new rows of one request and one query head
-// and walks that request's keys in 128-key tiles ("ORCA and chunked
-// prefill", section 4: a chunk of C rows attends to the S cached keys with
-// no mask and to its own C keys causally). Tiles that lie wholly above the
-// causal frontier of every row in the CTA are never visited; only tiles
-// that straddle it apply the mask (key j visible to new row i iff
-// j <= S0 + i, "How To Scale Your Model notes (7-8)", section 2).
+// One CTA owns up to 256 consecutive new rows of one request and one query
+// head, as two 128-row tiles A and B, and walks the request's keys in
+// 128-key tiles ("ORCA and chunked prefill", section 4: a chunk of C rows
+// attends to the S cached keys with no mask and to its own C keys causally).
+// A tile of keys that lies wholly above the causal frontier of every row of a
+// query tile is never computed for it; only key tiles that straddle the
+// frontier apply the mask (key j visible to new row i iff j <= S0 + i, "How To
+// Scale Your Model notes (7-8)", section 2).
 //
-// Data movement and roles (192 threads):
-//   warp 0      TMA producer: Q tile once (3-D tensor map over [total_q, Hq, D]),
-//               then K and V tiles page by page through the block table
-//               (2-D tensor map over the [pages * Hkv * page_size, D] cache
-//               view), 2-stage ring, 128-byte swizzle.
-//   warp 1      allocates 512 TMEM columns; one lane issues the MMAs:
-//               S = Q K^T (M 128, N 128, K = D) into a double-buffered TMEM
-//               score tile, O += P V (M 128, N = D, K 128) into the TMEM
-//               accumulator.
-//   warps 2-5   softmax, one thread per query row (TMEM lane = row): load the
-//               score row, mask, online max / sum in the log2 domain, write
-//               P (bf16, swizzled K-major) to shared memory, rescale O in
-//               TMEM only when the running max grew by more than 2^8, and at
-//               the end normalise O and store the bf16 row and its LSE.
+// Roles (320 threads):
+//   warp 0      TMA producer: both Q tiles once (3-D tensor map over
+//               [total_q, Hq, D]), then K_j, V_j, K_j+1, ... page by page
+//               through the block table (2-D tensor map over the
+//               [pages * Hkv * page_size, D] cache view) into a 3-slot ring
+//               shared by the two query tiles; 128-byte swizzle.
+//   warp 1      allocates all 512 TMEM columns (S_A, S_B, O_A, O_B); one lane
+//               issues every MMA: S_X = Q_X K^T (M 128, N 128, K = D) and
+//               O_X += P_X V (M 128, N = D, K 128), ordered
+//                   PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+//               so that each softmax group has two MMAs' time to turn its
+//               scores into probabilities while the tensor core works for the
+//               other group.
+//   warps 2-5   softmax of tile A, warps 6-9 softmax of tile B: one thread per
+//               query row (TMEM lane = row). Load the 128 scores of the row in
+//               one TMEM load, mask, take the running max (log2 domain, scale
+//               folded into one FFMA before ex2), write P as bf16 into shared
+//               memory in the K-major swizzled layout the MMA reads, and
+//               rescale O in TMEM only when a row's max grew by more than
+//               2^8. At the end normalise O and store the bf16 row and LSE.
 //
-// Every wait is bounded (see mb_device.cuh); on a timeout the CTA raises
-// its abort flag, drains the copies it issued, frees its TMEM and returns.
+// Every wait is bounded (see mb_device.cuh); on a timeout the CTA raises its
+// abort flag, drains the copies and MMAs it issued, frees its TMEM and returns.
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -37,48 +44,44 @@ namespace {
 
 using namespace dev;
 
-constexpr int BM = kPrefillTileM;
-constexpr int BN = kPrefillTileN;
-constexpr int kThreads = 192;
-constexpr int kStages = 2;
+constexpr int BM = kPrefillTileM;  // rows of one query tile
+constexpr int BN = kPrefillTileN;  // keys of one KV tile
+constexpr int kThreads = 320;
+constexpr int kSlots = 3;          // K/V ring slots
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr uint32_t kColS = 0;      // + 128 * tile
+constexpr uint32_t kColO = 256;    // + 128 * tile
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may reach 2^8 before O is rescaled
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint64_t kDrainNs = 200000000ull;
 
-// barrier slots
 enum {
   B_Q_FULL = 0,
-  B_K_FULL = 1,    // +stage
-  B_K_EMPTY = 3,   // +stage
-  B_V_FULL = 5,    // +stage
-  B_V_EMPTY = 7,   // +stage
-  B_S_FULL = 9,    // +buffer
-  B_S_FREE = 11,   // +buffer
-  B_P_FULL = 13,
-  B_PV_DONE = 14,
+  B_KV_FULL = 1,    // + slot
+  B_KV_EMPTY = 4,   // + slot
+  B_S_FULL = 7,     // + tile
+  B_S_FREE = 9,     // + tile
+  B_P_FULL = 11,    // + tile
+  B_O_DONE = 13,    // + tile
   B_VZ_READY = 15,
   B_COUNT = 16
 };
 
 template <int D>
 struct Layout {
-  static constexpr int kHalves = D / 64;                      // 64-element (128 B) column blocks
-  static constexpr uint32_t kHalfBytes = 128 * 128;           // 128 rows x 128 B
-  static constexpr uint32_t kQBytes = kHalves * kHalfBytes;
-  static constexpr uint32_t kKVBytes = kHalves * kHalfBytes;  // one stage of K (or V)
-  static constexpr uint32_t kPBytes = 2 * kHalfBytes;         // 128 keys = two 64-key blocks
-  static constexpr uint32_t q_off = 0;
-  static constexpr uint32_t k_off = q_off + kQBytes;
-  static constexpr uint32_t v_off = k_off + kStages * kKVBytes;
-  static constexpr uint32_t p_off = v_off + kStages * kKVBytes;
-  static constexpr uint32_t bar_off = p_off + kPBytes;
+  static constexpr int kHalves = D / 64;                       // 64-element (128 B) column blocks
+  static constexpr uint32_t kHalfBytes = 128 * 128;            // 128 rows x 128 B
+  static constexpr uint32_t kTileBytes = kHalves * kHalfBytes;  // a Q tile or a K/V slot
+  static constexpr uint32_t kPBytes = 2 * kHalfBytes;          // 128 keys = two 64-key blocks
+  static constexpr uint32_t q_off = 0;                         // Q_A, Q_B
+  static constexpr uint32_t kv_off = q_off + 2 * kTileBytes;   // 3 ring slots
+  static constexpr uint32_t p_off = kv_off + kSlots * kTileBytes;  // P_A, P_B
+  static constexpr uint32_t bar_off = p_off + 2 * kPBytes;
   static constexpr uint32_t misc_off = bar_off + B_COUNT * 8;
   static constexpr uint32_t kBytes = misc_off + 16;
-  // + alignment slack; at least 118 KB so that two CTAs never share an SM
-  // (each holds all 512 TMEM columns)
-  static constexpr uint32_t kAlloc = (kBytes + 1024 > 118u * 1024u) ? kBytes + 1024 : 118u * 1024u;
+  static constexpr uint32_t kAlloc = kBytes + 1024;  // + slack for 1024-byte alignment
+  static_assert(kAlloc <= 232448, "shared memory");
+  static_assert(kAlloc > 232448 / 2, "one CTA per SM (it holds all 512 TMEM columns)");
 };
 
 struct Params {
@@ -91,6 +94,8 @@ struct Params {
   int32_t* status;
 };
 
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const Params p, const __grid_constant__ CUtensorMap q_map,
@@ -101,8 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sq = smem + L::q_off;
-  uint8_t* sk = smem + L::k_off;
-  uint8_t* sv = smem + L::v_off;
+  uint8_t* skv = smem + L::kv_off;
   uint8_t* sp = smem + L::p_off;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
@@ -110,21 +114,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const PrefillItem it = p.items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_tiles = it.n_kv_tiles;
-  const bool tail_zero = n_tiles * BN > it.kv_length;  // last tile holds keys >= kv_length
+  const int rows_a = min(BM, it.n_rows);
+  const int rows_b = max(0, it.n_rows - BM);
+  // KV tiles each query tile needs (keys up to its last row's frontier)
+  const int nA = ceil_div(min(it.kv_length, it.s0 + it.i0 + rows_a), BN);
+  const int nB = rows_b > 0 ? ceil_div(min(it.kv_length, it.s0 + it.i0 + BM + rows_b), BN) : 0;
+  const int n = max(nA, nB);
+  const bool tail_zero = n * BN > it.kv_length;  // last KV tile holds keys >= kv_length
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_Q_FULL], 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars[B_K_FULL + s], 1);
-      mbar_init(&bars[B_K_EMPTY + s], 1);
-      mbar_init(&bars[B_V_FULL + s], 1);
-      mbar_init(&bars[B_V_EMPTY + s], 1);
-      mbar_init(&bars[B_S_FULL + s], 1);
-      mbar_init(&bars[B_S_FREE + s], 4);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&bars[B_KV_FULL + s], 1);
+      mbar_init(&bars[B_KV_EMPTY + s], 1);
     }
-    mbar_init(&bars[B_P_FULL], 4);
-    mbar_init(&bars[B_PV_DONE], 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars[B_S_FULL + t], 1);
+      mbar_init(&bars[B_S_FREE + t], 4);
+      mbar_init(&bars[B_P_FULL + t], 4);
+      mbar_init(&bars[B_O_DONE + t], 1);
+    }
     mbar_init(&bars[B_VZ_READY], 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -140,64 +149,61 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int last_issued = -1;
+    int issued = 0;  // ring items issued: K_j is item 2j, V_j item 2j + 1
     const int ps = 1 << p.ps_shift;
     if (lane == 0) {
       prefetch_tensormap(&q_map);
       prefetch_tensormap(&k_map);
       prefetch_tensormap(&v_map);
-      mbar_arrive_expect_tx(&bars[B_Q_FULL], L::kQBytes);
-      for (int h2 = 0; h2 < L::kHalves; ++h2)
-        tma_load_3d(sq + h2 * L::kHalfBytes, &q_map, &bars[B_Q_FULL], h2 * 64, it.q_head,
-                    it.q_row0);
+      mbar_arrive_expect_tx(&bars[B_Q_FULL], 2 * L::kTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int h2 = 0; h2 < L::kHalves; ++h2)
+          tma_load_3d(sq + t * L::kTileBytes + h2 * L::kHalfBytes, &q_map, &bars[B_Q_FULL],
+                      h2 * 64, it.q_head, it.q_row0 + t * BM);
       const int32_t* btrow = p.block_table + (int64_t)it.req * p.max_blocks;
       const int last_block = (it.kv_length - 1) >> p.ps_shift;
       const int kv_head = it.q_head / p.group;
-      for (int j = 0; j < n_tiles; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (j >= kStages && !mbar_wait(&bars[B_K_EMPTY + st], ph ^ 1, abort_flag, p.status))
+      int32_t ys[BN / 16];
+      for (int i = 0; i < 2 * n; ++i) {
+        const int j = i >> 1, slot = i % kSlots;
+        const uint32_t ph = (uint32_t)(i / kSlots) & 1u;
+        if (i >= kSlots && !mbar_wait(&bars[B_KV_EMPTY + slot], ph ^ 1u, abort_flag, p.status))
           break;
-        mbar_arrive_expect_tx(&bars[B_K_FULL + st], L::kKVBytes);
-        int32_t ys[BN / 16];
-        for (int pg = 0; pg < BN / ps; ++pg) {
-          int b = ((j * BN) >> p.ps_shift) + pg;
-          if (b > last_block) b = last_block;  // keys past kv_length: masked / zeroed
-          int32_t page = __ldg(btrow + b);
-          if ((unsigned)page >= (unsigned)p.num_pages) {
-            set_status(p.status, MB_ERR_DEVICE_INDEX);
-            page = 0;
+        if ((i & 1) == 0) {
+          for (int pg = 0; pg < BN / ps; ++pg) {
+            int b = ((j * BN) >> p.ps_shift) + pg;
+            if (b > last_block) b = last_block;  // keys past kv_length: masked, V zeroed
+            int32_t page = __ldg(btrow + b);
+            if ((unsigned)page >= (unsigned)p.num_pages) {
+              set_status(p.status, MB_ERR_DEVICE_INDEX);
+              page = 0;
+            }
+            ys[pg] = (page * p.n_kv_heads + kv_head) << p.ps_shift;
           }
-          ys[pg] = (page * p.n_kv_heads + kv_head) << p.ps_shift;
-          for (int h2 = 0; h2 < L::kHalves; ++h2)
-            tma_load_2d(sk + st * L::kKVBytes + h2 * L::kHalfBytes + pg * ps * 128, &k_map,
-                        &bars[B_K_FULL + st], h2 * 64, ys[pg]);
         }
-        if (j >= kStages && !mbar_wait(&bars[B_V_EMPTY + st], ph ^ 1, abort_flag, p.status)) {
-          last_issued = j;  // K of tile j is in flight
-          break;
-        }
-        mbar_arrive_expect_tx(&bars[B_V_FULL + st], L::kKVBytes);
+        const CUtensorMap* map = (i & 1) ? &v_map : &k_map;
+        uint8_t* dst = skv + slot * L::kTileBytes;
+        mbar_arrive_expect_tx(&bars[B_KV_FULL + slot], L::kTileBytes);
         for (int pg = 0; pg < BN / ps; ++pg)
           for (int h2 = 0; h2 < L::kHalves; ++h2)
-            tma_load_2d(sv + st * L::kKVBytes + h2 * L::kHalfBytes + pg * ps * 128, &v_map,
-                        &bars[B_V_FULL + st], h2 * 64, ys[pg]);
-        last_issued = j;
+            tma_load_2d(dst + h2 * L::kHalfBytes + pg * ps * 128, map, &bars[B_KV_FULL + slot],
+                        h2 * 64, ys[pg]);
+        issued = i + 1;
       }
     }
     __syncwarp();
-    last_issued = __shfl_sync(0xffffffffu, last_issued, 0);
-    if (tail_zero && last_issued == n_tiles - 1) {
-      // keys >= kv_length of the last tile: zero their V rows so that a
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+    if (tail_zero && issued == 2 * n) {
+      // keys >= kv_length in the last V tile: zero their rows so that a
       // non-finite value in an unwritten slot cannot reach O through P = 0
-      const int j = n_tiles - 1, st = j & 1;
-      const bool ok =
-          __all_sync(0xffffffffu, mbar_wait(&bars[B_V_FULL + st], (j >> 1) & 1, abort_flag,
-                                            p.status));
+      const int i = 2 * n - 1, slot = i % kSlots;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_KV_FULL + slot],
+                                                        (uint32_t)(i / kSlots) & 1u, abort_flag,
+                                                        p.status));
       if (ok) {
-        const int r0 = it.kv_length - j * BN;
+        const int r0 = it.kv_length - (n - 1) * BN;
         const int nz = BN - r0;
-        uint8_t* vb = sv + st * L::kKVBytes;
+        uint8_t* vb = skv + slot * L::kTileBytes;
         for (int idx = lane; idx < nz * L::kHalves * 8; idx += 32) {
           const int c = idx & 7;
           const int rr = idx >> 3;
@@ -212,13 +218,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[B_VZ_READY]);
     }
     if (lane == 0) {
-      // drain every copy still in flight before the CTA may exit
+      // every copy still in flight must land before the CTA may exit
       mbar_drain(&bars[B_Q_FULL], 0, kDrainNs);
-      for (int j = last_issued - 1; j <= last_issued; ++j) {
-        if (j < 0) continue;
-        mbar_drain(&bars[B_K_FULL + (j & 1)], (j >> 1) & 1, kDrainNs);
-        mbar_drain(&bars[B_V_FULL + (j & 1)], (j >> 1) & 1, kDrainNs);
-      }
+      for (int i = max(0, issued - kSlots); i < issued; ++i)
+        mbar_drain(&bars[B_KV_FULL + i % kSlots], (uint32_t)(i / kSlots) & 1u, kDrainNs);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -226,135 +229,162 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
       const uint32_t qa = smem_u32(sq);
+      const uint32_t kva = smem_u32(skv);
       const uint32_t pa = smem_u32(sp);
-      int last_pv = -1, last_s = -1;
-      auto issue_pv = [&](int t) -> bool {
-        const int st = t & 1;
-        if (!mbar_wait(&bars[B_P_FULL], t & 1, abort_flag, p.status)) return false;
-        if (!mbar_wait(&bars[B_V_FULL + st], (t >> 1) & 1, abort_flag, p.status)) return false;
-        if (t == n_tiles - 1 && tail_zero &&
-            !mbar_wait(&bars[B_VZ_READY], 0, abort_flag, p.status))
-          return false;
-        tc_fence_after();
-        const uint32_t va = smem_u32(sv + st * L::kKVBytes);
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // A = P [128 rows x 128 keys], K-major: 64-key block kk/4, 32 B step inside it
-          const uint64_t ad = sdesc_sw128(pa + (kk >> 2) * L::kHalfBytes + (kk & 3) * 32, 16, 1024);
-          // B = V [128 keys x D], MN-major: 16 keys = two 8-row groups (SBO 1024),
-          // next 64 head dims one half further (LBO)
-          const uint64_t bd = sdesc_sw128(va + kk * 2048, L::kHalfBytes, 1024);
-          umma_bf16_ss(tmem + kColO, ad, bd, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&bars[B_PV_DONE]);
-        umma_commit(&bars[B_V_EMPTY + st]);
-        last_pv = t;
-        return true;
-      };
-      bool ok = mbar_wait(&bars[B_Q_FULL], 0, abort_flag, p.status);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(&bars[B_K_FULL + st], (j >> 1) & 1, abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
-        if (j >= 2 && !mbar_wait(&bars[B_S_FREE + st], ((j - 2) >> 1) & 1, abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t ka = smem_u32(sk + st * L::kKVBytes);
+      int committed_o[2] = {-1, -1};
+      auto issue_s = [&](int t, int j) {
+        const uint32_t q0 = qa + t * L::kTileBytes;
+        const uint32_t k0 = kva + ((2 * j) % kSlots) * L::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
+          // K-major operands: 64-element block kk / 4, 32-byte step inside it
           const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-          umma_bf16_ss(tmem + (st ? kColS1 : kColS0), sdesc_sw128(qa + off, 16, 1024),
-                       sdesc_sw128(ka + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          umma_bf16_ss(tmem + kColS + 128 * t, sdesc_sw128(q0 + off, 16, 1024),
+                       sdesc_sw128(k0 + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bars[B_S_FULL + st]);
-        umma_commit(&bars[B_K_EMPTY + st]);
-        last_s = j;
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+        umma_commit(&bars[B_S_FULL + t]);
+      };
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t p0 = pa + t * L::kPBytes;
+        const uint32_t v0 = kva + ((2 * j + 1) % kSlots) * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          // A = P [128 rows x 128 keys], K-major; B = V [128 keys x D],
+          // MN-major: 16 keys = two 8-row groups (SBO), next 64 head dims
+          // one half further (LBO)
+          const uint64_t ad = sdesc_sw128(p0 + (kk >> 2) * L::kHalfBytes + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(v0 + kk * 2048, L::kHalfBytes, 1024);
+          umma_bf16_ss(tmem + kColO + 128 * t, ad, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&bars[B_O_DONE + t]);
+        committed_o[t] = j;
+      };
+      auto wait = [&](int b, uint32_t parity) -> bool {
+        const bool ok = mbar_wait(&bars[b], parity, abort_flag, p.status);
+        tc_fence_after();
+        return ok;
+      };
+      bool ok = wait(B_Q_FULL, 0);
+      if (ok && n > 0) {
+        ok = wait(B_KV_FULL + 0, 0);  // K_0
+        if (ok) {
+          if (nA > 0) issue_s(0, 0);
+          if (nB > 0) issue_s(1, 0);
+          umma_commit(&bars[B_KV_EMPTY + 0]);
+        }
       }
-      if (ok) issue_pv(n_tiles - 1);
-      // wait for the tensor core to finish what was issued
-      if (last_pv >= 0) mbar_drain(&bars[B_PV_DONE], last_pv & 1, kDrainNs);
-      if (last_s >= 0) mbar_drain(&bars[B_S_FULL + (last_s & 1)], (last_s >> 1) & 1, kDrainNs);
+      for (int j = 0; ok && j < n; ++j) {
+        const int vi = 2 * j + 1, ki = 2 * j + 2;
+        if (!(ok = wait(B_KV_FULL + vi % kSlots, (uint32_t)(vi / kSlots) & 1u))) break;
+        if (j == n - 1 && tail_zero && !(ok = wait(B_VZ_READY, 0))) break;
+        if (j < nA) {
+          if (!(ok = wait(B_P_FULL + 0, (uint32_t)j & 1u))) break;
+          issue_pv(0, j);
+        }
+        if (j + 1 < n && !(ok = wait(B_KV_FULL + ki % kSlots, (uint32_t)(ki / kSlots) & 1u)))
+          break;
+        if (j + 1 < nA) {
+          if (!(ok = wait(B_S_FREE + 0, (uint32_t)j & 1u))) break;
+          issue_s(0, j + 1);
+        }
+        if (j < nB) {
+          if (!(ok = wait(B_P_FULL + 1, (uint32_t)j & 1u))) break;
+          issue_pv(1, j);
+        }
+        umma_commit(&bars[B_KV_EMPTY + vi % kSlots]);  // V_j free once both PVs finish
+        if (j + 1 < nB) {
+          if (!(ok = wait(B_S_FREE + 1, (uint32_t)j & 1u))) break;
+          issue_s(1, j + 1);
+        }
+        if (j + 1 < n) umma_commit(&bars[B_KV_EMPTY + ki % kSlots]);  // K_j+1 after its S MMAs
+      }
+      // let the tensor core finish what was issued before the CTA exits
+      for (int t = 0; t < 2; ++t)
+        if (committed_o[t] >= 0)
+          mbar_drain(&bars[B_O_DONE + t], (uint32_t)committed_o[t] & 1u, kDrainNs);
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int wq = warp & 3;  // TMEM sub-partition this warp may access
-    const int r = wq * 32 + lane;
-    const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
-    const int vis_last = it.s0 + it.i0 + r;       // last key this row sees
-    const int tile_first_vis = it.s0 + it.i0;     // ... for the CTA's first row
-    float m = -INFINITY, l = 0.f;
+    const int t = (warp - 2) >> 2;     // query tile: warps 2-5 -> A, 6-9 -> B
+    const int sub = warp & 3;          // TMEM sub-partition this warp may access
+    const int r = sub * 32 + lane;     // row within the tile
+    const uint32_t lane_addr = (uint32_t)(sub * 32) << 16;
+    const uint32_t s_col = tmem + lane_addr + kColS + 128 * t;
+    const uint32_t o_col = tmem + lane_addr + kColO + 128 * t;
+    const int n_t = t ? nB : nA;
+    const int rows_t = t ? rows_b : rows_a;
+    const int first_vis = it.s0 + it.i0 + t * BM;  // last key visible to the tile's row 0
+    const int vis_last = first_vis + r;            // ... to this row
+    const float c = p.scale_log2;
+    uint8_t* prow = sp + t * L::kPBytes + r * 128;
+    float m = -INFINITY, l = 0.f;  // running max (raw score units), running sum
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int sb = j & 1;
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(&bars[B_S_FULL + sb], (j >> 1) & 1, abort_flag, p.status));
+    for (int j = 0; j < n_t; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_S_FULL + t], (uint32_t)j & 1u, abort_flag,
+                                             p.status));
       if (!ok) break;
       tc_fence_after();
-      uint32_t s[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(tmem + lane_addr + (sb ? kColS1 : kColS0) + c * 32, s[c]);
-        tmem_ld_wait(s[c]);
-      }
+      uint32_t s[128];
+      tmem_ld128(s_col, s);
+      tmem_ld_wait128(s);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_S_FREE + sb]);
+      if (lane == 0) mbar_arrive(&bars[B_S_FREE + t]);
 
       const int key0 = j * BN;
-      const bool need_mask = key0 + BN - 1 > tile_first_vis;
-      float mt = -INFINITY;
+      if (key0 + BN - 1 > first_vis) {  // tile straddles the causal frontier
+        const int lim = vis_last - key0;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+        for (int e = 0; e < 128; ++e)
+          if (e > lim) s[e] = __float_as_uint(-INFINITY);
+      }
+      float mx[8];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float v = __uint_as_float(s[c][e]) * p.scale_log2;
-          if (need_mask && key0 + c * 32 + e > vis_last) v = -INFINITY;
-          s[c][e] = __float_as_uint(v);
-          mt = fmaxf(mt, v);
-        }
-      const float m_new = fmaxf(m, mt);
-      if (j >= 1) {
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(&bars[B_PV_DONE], (j - 1) & 1, abort_flag, p.status));
+      for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(s[k]);
+#pragma unroll
+      for (int e = 8; e < 128; e += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(s[e + k]));
+      const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float m_new = fmaxf(m, tmax);
+      if (j > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + t], (uint32_t)(j - 1) & 1u,
+                                               abort_flag, p.status));
         if (!ok) break;
       }
       if (j == 0) {
         m = m_new;
       } else {
-        const bool need = m_new > m + kRescaleThreshold;
+        const bool need = (m_new - m) * c > kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? fast_exp2(m - m_new) : 1.f;
+          const float alpha = need ? fast_exp2((m - m_new) * c) : 1.f;
           if (need) {
             l *= alpha;
             m = m_new;
           }
           tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+          for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t o[32];
-            tmem_ld32(tmem + lane_addr + kColO + c * 32, o);
+            tmem_ld32(o_col + cc * 32, o);
             tmem_ld_wait(o);
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tmem + lane_addr + kColO + c * 32, o);
+            tmem_st32(o_col + cc * 32, o);
           }
           tmem_st_wait();
         }
       }
-      const float mx = (m == -INFINITY) ? 0.f : m;
-      float rowsum = 0.f;
+      const float mc = (m == -INFINITY) ? 0.f : m * c;
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int ch = 0; ch < BN / 8; ++ch) {
         float e8[8];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          e8[t] = fast_exp2(__uint_as_float(s[ch >> 2][(ch & 3) * 8 + t]) - mx);
-          rowsum += e8[t];
+        for (int k = 0; k < 8; ++k) {
+          e8[k] = fast_exp2(fmaf(__uint_as_float(s[ch * 8 + k]), c, -mc));
+          sum[k & 3] += e8[k];
         }
         uint4 pk;
         pk.x = pack_bf16x2(e8[0], e8[1]);
@@ -362,28 +392,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk.z = pack_bf16x2(e8[4], e8[5]);
         pk.w = pack_bf16x2(e8[6], e8[7]);
         const int half = ch >> 3, c8 = ch & 7;
-        *reinterpret_cast<uint4*>(sp + half * L::kHalfBytes + r * 128 + ((c8 ^ (r & 7)) << 4)) =
-            pk;
+        *reinterpret_cast<uint4*>(prow + half * L::kHalfBytes + ((c8 ^ (r & 7)) << 4)) = pk;
       }
-      l += rowsum;
+      l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_P_FULL]);
+      if (lane == 0) mbar_arrive(&bars[B_P_FULL + t]);
     }
-    if (ok)
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_PV_DONE], (n_tiles - 1) & 1, abort_flag,
-                                             p.status));
-    if (ok) {
+    if (ok && n_t > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + t], (uint32_t)(n_t - 1) & 1u,
+                                             abort_flag, p.status));
+    if (ok && n_t > 0) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const bool valid = r < it.n_rows;
-      const int64_t orow = (int64_t)(it.q_row0 + r) * p.n_q_heads + it.q_head;
+      const bool valid = r < rows_t;
+      const int64_t orow = (int64_t)(it.q_row0 + t * BM + r) * p.n_q_heads + it.q_head;
       uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_addr + kColO + c * 32, o);
+        tmem_ld32(o_col + cc * 32, o);
         tmem_ld_wait(o);
         if (valid) {
 #pragma unroll
@@ -393,11 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
             v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
             v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
-            dst[c * 4 + q4] = v;
+            dst[cc * 4 + q4] = v;
           }
         }
       }
-      if (valid && p.lse) p.lse[orow] = (m + log2f(l)) * kLn2;
+      if (valid && p.lse) p.lse[orow] = (m * c + log2f(l)) * kLn2;
     }
   }
 
@@ -417,13 +446,13 @@ cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
   p.max_blocks = a.max_blocks;
   p.n_q_heads = a.n_q_heads;
   p.n_kv_heads = a.n_kv_heads;
+  p.num_pages = a.num_pages;
   p.group = a.n_q_heads / a.n_kv_heads;
   p.ps_shift = __builtin_ctz((unsigned)a.page_size);
   p.scale_log2 = a.scale_log2;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
   p.status = a.status;
-  p.num_pages = a.num_pages;
   constexpr uint32_t smem = Layout<D>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);

@@ -153,7 +153,7 @@ def check_coverage(w, opts=None):
                  int(it["bt_row"])))
     pcover = {}
     for p in pitems:
-        assert 1 <= p["n_rows"] <= 128
+        assert 1 <= p["n_rows"] <= 256
         for i in range(p["n_rows"]):
             key = (int(p["q_row0"]) + i, int(p["q_head"]))
             assert key not in pcover
@@ -223,12 +223,13 @@ def test_planner_coverage_options(L, name, opts):
 
 
 def test_prefill_tiles_skip_masked_tiles(L):
-    # one 4096-row prefill: tile t of 128 rows visits exactly t + 1 KV tiles
+    # one 4096-row prefill: CTA t owns rows [256 t, 256 t + 256) and visits
+    # exactly the 2 t + 2 KV tiles of 128 keys its last row can see
     w = W.make_workload("llama2_7b_orca_iteration", with_values=False)
     hp = B.HostPlan(w.requests, w.block_table, cfg_for(w))
     _, _, pitems, _ = decode_plan(hp)
     a = pitems[pitems["req"] == 0]
-    assert len(a) == 32 * 32
-    assert sorted(set((a["i0"] // 128 + 1 - a["n_kv_tiles"]).tolist())) == [0]
+    assert len(a) == 32 * 16
+    assert sorted(set((2 * (a["i0"] // 256) + 2 - a["n_kv_tiles"]).tolist())) == [0]
     # heaviest first
     assert np.all(np.diff(pitems["n_kv_tiles"]) <= 0)

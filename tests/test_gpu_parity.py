@@ -99,7 +99,7 @@ def test_llama_iteration_parity_sampled():
     w = W.make_workload("llama2_7b_orca_iteration")
     kc, vc, cfg = fill_cache(w)
     out, lse, status, info = run_forward(w, kc, vc, cfg)
-    assert status == 0 and info["n_prefill_items"] == 32 * 32
+    assert status == 0 and info["n_prefill_items"] == 32 * 16
     assert torch.isfinite(out.float()).all()
     # the 4096-row prefill: three heads in full (every tile, ragged-free)
     assert_request_close(w, out, lse, 0, heads=[0, 13, 31])
