@@ -140,6 +140,19 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// ---------------------------------------------------------------- registers
+// Warpgroup-wide register re-allocation (every warp of the warpgroup executes
+// it). An increase waits until the registers are free, so the sum over the
+// warpgroups must stay within the registers the CTA was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- tcgen05
 // TMEM allocation (one full warp executes these).
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {

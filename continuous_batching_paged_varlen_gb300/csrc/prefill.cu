@@ -9,26 +9,33 @@
 // frontier apply the mask (key j visible to new row i iff j <= S0 + i, "How To
 // Scale Your Model notes (7-8)", section 2).
 //
-// Roles (320 threads):
-//   warp 0      TMA producer: both Q tiles once (3-D tensor map over
+// Roles (384 threads, three warpgroups):
+//   warps 0-3   softmax of query tile A, warps 4-7 softmax of tile B: one
+//               thread per query row (TMEM lane = row). Load the 128 scores of
+//               the row in one TMEM load, mask, take the running max (log2
+//               domain, scale folded into one FFMA before ex2), write P as
+//               bf16 into shared memory in the K-major swizzled layout the
+//               MMA reads, and rescale O in TMEM only when a row's max grew
+//               by more than 2^8. The two groups share one P buffer and hand
+//               it over in the order the MMAs read it (P_A(j), P_B(j),
+//               P_A(j+1), ...). At the end normalise O and store the bf16 row
+//               and its LSE. These warpgroups take registers from the third
+//               one (setmaxnreg) so the 128 scores of a row stay in registers.
+//   warp 8      TMA producer: both Q tiles once (3-D tensor map over
 //               [total_q, Hq, D]), then K_j, V_j, K_j+1, ... page by page
 //               through the block table (2-D tensor map over the
-//               [pages * Hkv * page_size, D] cache view) into a 3-slot ring
-//               shared by the two query tiles; 128-byte swizzle.
-//   warp 1      allocates all 512 TMEM columns (S_A, S_B, O_A, O_B); one lane
+//               [pages * Hkv * page_size, D] cache view) into a 4-slot ring
+//               shared by the two query tiles; 128-byte swizzle. Each lane
+//               looks up one page and issues that page's boxes, so a tile of
+//               16-token pages is in flight after one round of issues.
+//   warp 9      allocates all 512 TMEM columns (S_A, S_B, O_A, O_B); one lane
 //               issues every MMA: S_X = Q_X K^T (M 128, N 128, K = D) and
 //               O_X += P_X V (M 128, N = D, K 128), ordered
 //                   PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
 //               so that each softmax group has two MMAs' time to turn its
 //               scores into probabilities while the tensor core works for the
 //               other group.
-//   warps 2-5   softmax of tile A, warps 6-9 softmax of tile B: one thread per
-//               query row (TMEM lane = row). Load the 128 scores of the row in
-//               one TMEM load, mask, take the running max (log2 domain, scale
-//               folded into one FFMA before ex2), write P as bf16 into shared
-//               memory in the K-major swizzled layout the MMA reads, and
-//               rescale O in TMEM only when a row's max grew by more than
-//               2^8. At the end normalise O and store the bf16 row and LSE.
+//   warps 10-11 idle.
 //
 // Every wait is bounded (see mb_device.cuh); on a timeout the CTA raises its
 // abort flag, drains the copies and MMAs it issued, frees its TMEM and returns.
@@ -46,8 +53,15 @@ using namespace dev;
 
 constexpr int BM = kPrefillTileM;  // rows of one query tile
 constexpr int BN = kPrefillTileN;  // keys of one KV tile
-constexpr int kThreads = 320;
-constexpr int kSlots = 3;          // K/V ring slots
+constexpr int kThreads = 384;
+// registers per thread: at launch (ptxas' count under the launch bounds, checked
+// on the host before every launch), then after the re-allocation
+constexpr int kLaunchRegs = 168;
+constexpr int kProducerRegs = 56;
+constexpr int kSoftmaxRegs = 224;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kProducerRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch's register pool");
+constexpr int kSlots = 4;          // K/V ring slots
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;      // + 128 * tile
 constexpr uint32_t kColO = 256;    // + 128 * tile
@@ -58,13 +72,13 @@ constexpr uint64_t kDrainNs = 200000000ull;
 enum {
   B_Q_FULL = 0,
   B_KV_FULL = 1,    // + slot
-  B_KV_EMPTY = 4,   // + slot
-  B_S_FULL = 7,     // + tile
-  B_S_FREE = 9,     // + tile
-  B_P_FULL = 11,    // + tile
-  B_O_DONE = 13,    // + tile
-  B_VZ_READY = 15,
-  B_COUNT = 16
+  B_KV_EMPTY = 5,   // + slot
+  B_S_FULL = 9,     // + tile
+  B_S_FREE = 11,    // + tile
+  B_P_FULL = 13,    // + tile
+  B_O_DONE = 15,    // + tile
+  B_VZ_READY = 17,
+  B_COUNT = 18
 };
 
 template <int D>
@@ -74,9 +88,9 @@ struct Layout {
   static constexpr uint32_t kTileBytes = kHalves * kHalfBytes;  // a Q tile or a K/V slot
   static constexpr uint32_t kPBytes = 2 * kHalfBytes;          // 128 keys = two 64-key blocks
   static constexpr uint32_t q_off = 0;                         // Q_A, Q_B
-  static constexpr uint32_t kv_off = q_off + 2 * kTileBytes;   // 3 ring slots
-  static constexpr uint32_t p_off = kv_off + kSlots * kTileBytes;  // P_A, P_B
-  static constexpr uint32_t bar_off = p_off + 2 * kPBytes;
+  static constexpr uint32_t kv_off = q_off + 2 * kTileBytes;   // ring slots
+  static constexpr uint32_t p_off = kv_off + kSlots * kTileBytes;  // one P buffer
+  static constexpr uint32_t bar_off = p_off + kPBytes;
   static constexpr uint32_t misc_off = bar_off + B_COUNT * 8;
   static constexpr uint32_t kBytes = misc_off + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // + slack for 1024-byte alignment
@@ -138,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 1) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -147,10 +161,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp >= 8) {
+    regs_dec<kProducerRegs>();
+  }
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     int issued = 0;  // ring items issued: K_j is item 2j, V_j item 2j + 1
     const int ps = 1 << p.ps_shift;
+    const int npg = BN / ps;                    // pages per KV tile
+    const int nbox = npg * L::kHalves;          // TMA boxes per K or V tile (<= 16)
     if (lane == 0) {
       prefetch_tensormap(&q_map);
       prefetch_tensormap(&k_map);
@@ -160,39 +179,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h2 = 0; h2 < L::kHalves; ++h2)
           tma_load_3d(sq + t * L::kTileBytes + h2 * L::kHalfBytes, &q_map, &bars[B_Q_FULL],
                       h2 * 64, it.q_head, it.q_row0 + t * BM);
-      const int32_t* btrow = p.block_table + (int64_t)it.req * p.max_blocks;
-      const int last_block = (it.kv_length - 1) >> p.ps_shift;
-      const int kv_head = it.q_head / p.group;
-      int32_t ys[BN / 16];
-      for (int i = 0; i < 2 * n; ++i) {
-        const int j = i >> 1, slot = i % kSlots;
-        const uint32_t ph = (uint32_t)(i / kSlots) & 1u;
-        if (i >= kSlots && !mbar_wait(&bars[B_KV_EMPTY + slot], ph ^ 1u, abort_flag, p.status))
-          break;
-        if ((i & 1) == 0) {
-          for (int pg = 0; pg < BN / ps; ++pg) {
-            int b = ((j * BN) >> p.ps_shift) + pg;
-            if (b > last_block) b = last_block;  // keys past kv_length: masked, V zeroed
-            int32_t page = __ldg(btrow + b);
-            if ((unsigned)page >= (unsigned)p.num_pages) {
-              set_status(p.status, MB_ERR_DEVICE_INDEX);
-              page = 0;
-            }
-            ys[pg] = (page * p.n_kv_heads + kv_head) << p.ps_shift;
-          }
+    }
+    const int32_t* btrow = p.block_table + (int64_t)it.req * p.max_blocks;
+    const int last_block = (it.kv_length - 1) >> p.ps_shift;
+    const int kv_head = it.q_head / p.group;
+    // lane l issues box (page l % npg, column block l / npg) of every tile
+    const int my_pg = lane % npg, my_h2 = lane / npg;
+    int32_t my_y = 0;
+    for (int i = 0; i < 2 * n; ++i) {
+      const int j = i >> 1, slot = i % kSlots;
+      const uint32_t ph = (uint32_t)(i / kSlots) & 1u;
+      if (i >= kSlots &&
+          !__all_sync(0xffffffffu, mbar_wait(&bars[B_KV_EMPTY + slot], ph ^ 1u, abort_flag,
+                                             p.status)))
+        break;
+      if ((i & 1) == 0 && lane < npg) {  // page of this lane for K_j and V_j
+        int b = ((j * BN) >> p.ps_shift) + lane;
+        if (b > last_block) b = last_block;  // keys past kv_length: masked, V zeroed
+        int32_t page = __ldg(btrow + b);
+        if ((unsigned)page >= (unsigned)p.num_pages) {
+          set_status(p.status, MB_ERR_DEVICE_INDEX);
+          page = 0;
         }
-        const CUtensorMap* map = (i & 1) ? &v_map : &k_map;
-        uint8_t* dst = skv + slot * L::kTileBytes;
-        mbar_arrive_expect_tx(&bars[B_KV_FULL + slot], L::kTileBytes);
-        for (int pg = 0; pg < BN / ps; ++pg)
-          for (int h2 = 0; h2 < L::kHalves; ++h2)
-            tma_load_2d(dst + h2 * L::kHalfBytes + pg * ps * 128, map, &bars[B_KV_FULL + slot],
-                        h2 * 64, ys[pg]);
-        issued = i + 1;
+        my_y = (page * p.n_kv_heads + kv_head) << p.ps_shift;
       }
+      const int32_t y = __shfl_sync(0xffffffffu, my_y, my_pg);
+      if (lane == 0) mbar_arrive_expect_tx(&bars[B_KV_FULL + slot], L::kTileBytes);
+      __syncwarp();
+      if (lane < nbox)
+        tma_load_2d(skv + slot * L::kTileBytes + my_h2 * L::kHalfBytes + my_pg * ps * 128,
+                    (i & 1) ? &v_map : &k_map, &bars[B_KV_FULL + slot], my_h2 * 64, y);
+      issued = i + 1;
     }
     __syncwarp();
-    issued = __shfl_sync(0xffffffffu, issued, 0);
     if (tail_zero && issued == 2 * n) {
       // keys >= kv_length in the last V tile: zero their rows so that a
       // non-finite value in an unwritten slot cannot reach O through P = 0
@@ -223,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = max(0, issued - kSlots); i < issued; ++i)
         mbar_drain(&bars[B_KV_FULL + i % kSlots], (uint32_t)(i / kSlots) & 1u, kDrainNs);
     }
-  } else if (warp == 1) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
@@ -245,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&bars[B_S_FULL + t]);
       };
       auto issue_pv = [&](int t, int j) {
-        const uint32_t p0 = pa + t * L::kPBytes;
+        const uint32_t p0 = pa;
         const uint32_t v0 = kva + ((2 * j + 1) % kSlots) * L::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
@@ -303,9 +322,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (committed_o[t] >= 0)
           mbar_drain(&bars[B_O_DONE + t], (uint32_t)committed_o[t] & 1u, kDrainNs);
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
-    const int t = (warp - 2) >> 2;     // query tile: warps 2-5 -> A, 6-9 -> B
+    regs_inc<kSoftmaxRegs>();
+    const int t = warp >> 2;           // query tile: warps 0-3 -> A, 4-7 -> B
     const int sub = warp & 3;          // TMEM sub-partition this warp may access
     const int r = sub * 32 + lane;     // row within the tile
     const uint32_t lane_addr = (uint32_t)(sub * 32) << 16;
@@ -316,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int first_vis = it.s0 + it.i0 + t * BM;  // last key visible to the tile's row 0
     const int vis_last = first_vis + r;            // ... to this row
     const float c = p.scale_log2;
-    uint8_t* prow = sp + t * L::kPBytes + r * 128;
+    uint8_t* prow = sp + r * 128;
     float m = -INFINITY, l = 0.f;  // running max (raw score units), running sum
     bool ok = true;
     for (int j = 0; j < n_t; ++j) {
@@ -338,61 +358,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 128; ++e)
           if (e > lim) s[e] = __float_as_uint(-INFINITY);
       }
-      float mx[8];
+      float mx[16];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(s[k]);
+      for (int k = 0; k < 16; ++k) mx[k] = __uint_as_float(s[k]);
 #pragma unroll
-      for (int e = 8; e < 128; e += 8)
+      for (int e = 16; e < 128; e += 16)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(s[e + k]));
-      const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int k = 0; k < 16; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(s[e + k]));
+#pragma unroll
+      for (int w2 = 8; w2 > 0; w2 >>= 1)
+#pragma unroll
+        for (int k = 0; k < w2; ++k) mx[k] = fmaxf(mx[k], mx[k + w2]);
+      const float tmax = mx[0];
       const float m_new = fmaxf(m, tmax);
-      if (j > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + t], (uint32_t)(j - 1) & 1u,
-                                               abort_flag, p.status));
-        if (!ok) break;
-      }
+      // lazy rescale: keep the old max unless it grew by more than 2^8
+      float alpha = 1.f;
+      bool need = false;
       if (j == 0) {
         m = m_new;
       } else {
-        const bool need = (m_new - m) * c > kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? fast_exp2((m - m_new) * c) : 1.f;
-          if (need) {
-            l *= alpha;
-            m = m_new;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(o_col + cc * 32, o);
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(o_col + cc * 32, o);
-          }
-          tmem_st_wait();
+        need = (m_new - m) * c > kRescaleThreshold;
+        if (need) {
+          alpha = fast_exp2((m - m_new) * c);
+          l *= alpha;
+          m = m_new;
         }
       }
       const float mc = (m == -INFINITY) ? 0.f : m * c;
       float sum[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[64];
+#pragma unroll
+      for (int e = 0; e < 128; e += 2) {
+        const float e0 = fast_exp2(fmaf(__uint_as_float(s[e]), c, -mc));
+        const float e1 = fast_exp2(fmaf(__uint_as_float(s[e + 1]), c, -mc));
+        sum[(e >> 1) & 3] += e0 + e1;
+        pk[e >> 1] = pack_bf16x2(e0, e1);
+      }
+      // the P buffer (and O_t) are free once the previous PV in MMA order is done:
+      // for A(j) that is PV_B(j-1) (or PV_A(j-1) without B), for B(j) it is
+      // PV_A(j) (or PV_B(j-1) once A has no tile j)
+      int wb = -1;
+      uint32_t wpar = 0;
+      if (t == 0) {
+        if (j > 0) {
+          if (j - 1 < nB) { wb = B_O_DONE + 1; wpar = (uint32_t)(j - 1) & 1u; }
+          else { wb = B_O_DONE + 0; wpar = (uint32_t)(j - 1) & 1u; }
+        }
+      } else {
+        if (j < nA) { wb = B_O_DONE + 0; wpar = (uint32_t)j & 1u; }
+        else if (j > 0) { wb = B_O_DONE + 1; wpar = (uint32_t)(j - 1) & 1u; }
+      }
+      if (wb >= 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars[wb], wpar, abort_flag, p.status));
+        if (!ok) break;
+      }
+      if (__any_sync(0xffffffffu, need)) {
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(o_col + cc * 32, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(o_col + cc * 32, o);
+        }
+        tmem_st_wait();
+      }
 #pragma unroll
       for (int ch = 0; ch < BN / 8; ++ch) {
-        float e8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          e8[k] = fast_exp2(fmaf(__uint_as_float(s[ch * 8 + k]), c, -mc));
-          sum[k & 3] += e8[k];
-        }
-        uint4 pk;
-        pk.x = pack_bf16x2(e8[0], e8[1]);
-        pk.y = pack_bf16x2(e8[2], e8[3]);
-        pk.z = pack_bf16x2(e8[4], e8[5]);
-        pk.w = pack_bf16x2(e8[6], e8[7]);
         const int half = ch >> 3, c8 = ch & 7;
-        *reinterpret_cast<uint4*>(prow + half * L::kHalfBytes + ((c8 ^ (r & 7)) << 4)) = pk;
+        *reinterpret_cast<uint4*>(prow + half * L::kHalfBytes + ((c8 ^ (r & 7)) << 4)) =
+            make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
       }
       l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
       fence_proxy_async_smem();
@@ -432,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -454,7 +491,13 @@ cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
   p.lse = a.lse;
   p.status = a.status;
   constexpr uint32_t smem = Layout<D>::kAlloc;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // the register split assumes the kernel launches with kLaunchRegs per thread;
+  // with fewer, a warpgroup's increase could never be satisfied
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   prefill_kernel<D><<<a.n_items, kThreads, smem, s>>>(p, *a.q_map, *a.k_map, *a.v_map);
