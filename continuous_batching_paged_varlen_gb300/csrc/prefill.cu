@@ -14,27 +14,28 @@
 //               thread per query row (TMEM lane = row). Load the 128 scores of
 //               the row in one TMEM load, mask, take the running max (log2
 //               domain, scale folded into one FFMA before ex2), write P as
-//               bf16 into shared memory in the K-major swizzled layout the
-//               MMA reads, and rescale O in TMEM only when a row's max grew
-//               by more than 2^8. The two groups share one P buffer and hand
-//               it over in the order the MMAs read it (P_A(j), P_B(j),
-//               P_A(j+1), ...). At the end normalise O and store the bf16 row
-//               and its LSE. These warpgroups take registers from the third
-//               one (setmaxnreg) so the 128 scores of a row stay in registers.
+//               bf16 back into TMEM over the row's own scores (the PV MMA
+//               reads its A operand from there), and rescale O in TMEM only
+//               when a row's max grew by more than 2^8. At the end normalise
+//               O and store the bf16 row and its LSE. These warpgroups take
+//               registers from the third one (setmaxnreg) so the 128 scores of
+//               a row stay in registers.
 //   warp 8      TMA producer: both Q tiles once (3-D tensor map over
 //               [total_q, Hq, D]), then K_j, V_j, K_j+1, ... page by page
 //               through the block table (2-D tensor map over the
-//               [pages * Hkv * page_size, D] cache view) into a 4-slot ring
+//               [pages * Hkv * page_size, D] cache view) into a 5/6-slot ring
 //               shared by the two query tiles; 128-byte swizzle. Each lane
 //               looks up one page and issues that page's boxes, so a tile of
 //               16-token pages is in flight after one round of issues.
 //   warp 9      allocates all 512 TMEM columns (S_A, S_B, O_A, O_B); one lane
-//               issues every MMA: S_X = Q_X K^T (M 128, N 128, K = D) and
-//               O_X += P_X V (M 128, N = D, K 128), ordered
+//               issues every MMA: S_X = Q_X K^T (M 128, N 128, K = D, both
+//               operands in shared memory) and O_X += P_X V (M 128, N = D,
+//               K 128, P from TMEM, V from shared memory), ordered
 //                   PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
 //               so that each softmax group has two MMAs' time to turn its
 //               scores into probabilities while the tensor core works for the
-//               other group.
+//               other group. S_X(j+1) overwrites the columns PV_X(j) reads P
+//               from; the tensor core runs one thread's MMAs in issue order.
 //   warps 10-11 idle.
 //
 // Every wait is bounded (see mb_device.cuh); on a timeout the CTA raises its
@@ -61,7 +62,6 @@ constexpr int kProducerRegs = 56;
 constexpr int kSoftmaxRegs = 224;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kProducerRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch's register pool");
-constexpr int kSlots = 4;          // K/V ring slots
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;      // + 128 * tile
 constexpr uint32_t kColO = 256;    // + 128 * tile
@@ -70,15 +70,15 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint64_t kDrainNs = 200000000ull;
 
 enum {
+  kMaxSlots = 6,
   B_Q_FULL = 0,
-  B_KV_FULL = 1,    // + slot
-  B_KV_EMPTY = 5,   // + slot
-  B_S_FULL = 9,     // + tile
-  B_S_FREE = 11,    // + tile
-  B_P_FULL = 13,    // + tile
-  B_O_DONE = 15,    // + tile
-  B_VZ_READY = 17,
-  B_COUNT = 18
+  B_KV_FULL = 1,                  // + slot
+  B_KV_EMPTY = 1 + kMaxSlots,     // + slot
+  B_S_FULL = 1 + 2 * kMaxSlots,   // + tile
+  B_P_FULL = 3 + 2 * kMaxSlots,   // + tile
+  B_O_DONE = 5 + 2 * kMaxSlots,   // + tile
+  B_VZ_READY = 7 + 2 * kMaxSlots,
+  B_COUNT = 8 + 2 * kMaxSlots
 };
 
 template <int D>
@@ -86,11 +86,11 @@ struct Layout {
   static constexpr int kHalves = D / 64;                       // 64-element (128 B) column blocks
   static constexpr uint32_t kHalfBytes = 128 * 128;            // 128 rows x 128 B
   static constexpr uint32_t kTileBytes = kHalves * kHalfBytes;  // a Q tile or a K/V slot
-  static constexpr uint32_t kPBytes = 2 * kHalfBytes;          // 128 keys = two 64-key blocks
+  static constexpr int kSlots = D == 128 ? 5 : 6;               // K/V ring slots
+  static_assert(kSlots <= kMaxSlots, "barrier slots");
   static constexpr uint32_t q_off = 0;                         // Q_A, Q_B
   static constexpr uint32_t kv_off = q_off + 2 * kTileBytes;   // ring slots
-  static constexpr uint32_t p_off = kv_off + kSlots * kTileBytes;  // one P buffer
-  static constexpr uint32_t bar_off = p_off + kPBytes;
+  static constexpr uint32_t bar_off = kv_off + kSlots * kTileBytes;
   static constexpr uint32_t misc_off = bar_off + B_COUNT * 8;
   static constexpr uint32_t kBytes = misc_off + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // + slack for 1024-byte alignment
@@ -121,7 +121,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sq = smem + L::q_off;
   uint8_t* skv = smem + L::kv_off;
-  uint8_t* sp = smem + L::p_off;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
@@ -138,13 +137,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_Q_FULL], 1);
-    for (int s = 0; s < kSlots; ++s) {
+    for (int s = 0; s < L::kSlots; ++s) {
       mbar_init(&bars[B_KV_FULL + s], 1);
       mbar_init(&bars[B_KV_EMPTY + s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars[B_S_FULL + t], 1);
-      mbar_init(&bars[B_S_FREE + t], 4);
       mbar_init(&bars[B_P_FULL + t], 4);
       mbar_init(&bars[B_O_DONE + t], 1);
     }
@@ -187,9 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int my_pg = lane % npg, my_h2 = lane / npg;
     int32_t my_y = 0;
     for (int i = 0; i < 2 * n; ++i) {
-      const int j = i >> 1, slot = i % kSlots;
-      const uint32_t ph = (uint32_t)(i / kSlots) & 1u;
-      if (i >= kSlots &&
+      const int j = i >> 1, slot = i % L::kSlots;
+      const uint32_t ph = (uint32_t)(i / L::kSlots) & 1u;
+      if (i >= L::kSlots &&
           !__all_sync(0xffffffffu, mbar_wait(&bars[B_KV_EMPTY + slot], ph ^ 1u, abort_flag,
                                              p.status)))
         break;
@@ -215,9 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tail_zero && issued == 2 * n) {
       // keys >= kv_length in the last V tile: zero their rows so that a
       // non-finite value in an unwritten slot cannot reach O through P = 0
-      const int i = 2 * n - 1, slot = i % kSlots;
+      const int i = 2 * n - 1, slot = i % L::kSlots;
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_KV_FULL + slot],
-                                                        (uint32_t)(i / kSlots) & 1u, abort_flag,
+                                                        (uint32_t)(i / L::kSlots) & 1u, abort_flag,
                                                         p.status));
       if (ok) {
         const int r0 = it.kv_length - (n - 1) * BN;
@@ -239,8 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // every copy still in flight must land before the CTA may exit
       mbar_drain(&bars[B_Q_FULL], 0, kDrainNs);
-      for (int i = max(0, issued - kSlots); i < issued; ++i)
-        mbar_drain(&bars[B_KV_FULL + i % kSlots], (uint32_t)(i / kSlots) & 1u, kDrainNs);
+      for (int i = max(0, issued - L::kSlots); i < issued; ++i)
+        mbar_drain(&bars[B_KV_FULL + i % L::kSlots], (uint32_t)(i / L::kSlots) & 1u, kDrainNs);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -249,11 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
       const uint32_t qa = smem_u32(sq);
       const uint32_t kva = smem_u32(skv);
-      const uint32_t pa = smem_u32(sp);
       int committed_o[2] = {-1, -1};
       auto issue_s = [&](int t, int j) {
         const uint32_t q0 = qa + t * L::kTileBytes;
-        const uint32_t k0 = kva + ((2 * j) % kSlots) * L::kTileBytes;
+        const uint32_t k0 = kva + ((2 * j) % L::kSlots) * L::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // K-major operands: 64-element block kk / 4, 32-byte step inside it
@@ -264,16 +261,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&bars[B_S_FULL + t]);
       };
       auto issue_pv = [&](int t, int j) {
-        const uint32_t p0 = pa;
-        const uint32_t v0 = kva + ((2 * j + 1) % kSlots) * L::kTileBytes;
+        const uint32_t v0 = kva + ((2 * j + 1) % L::kSlots) * L::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          // A = P [128 rows x 128 keys], K-major; B = V [128 keys x D],
-          // MN-major: 16 keys = two 8-row groups (SBO), next 64 head dims
-          // one half further (LBO)
-          const uint64_t ad = sdesc_sw128(p0 + (kk >> 2) * L::kHalfBytes + (kk & 3) * 32, 16, 1024);
+          // A = P [128 rows x 128 keys] in TMEM over S_X: 16 keys = 8 columns;
+          // B = V [128 keys x D], MN-major: 16 keys = two 8-row groups (SBO),
+          // next 64 head dims one half further (LBO)
           const uint64_t bd = sdesc_sw128(v0 + kk * 2048, L::kHalfBytes, 1024);
-          umma_bf16_ss(tmem + kColO + 128 * t, ad, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + kColO + 128 * t, tmem + kColS + 128 * t + kk * 8, bd, idesc_pv,
+                       (j > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&bars[B_O_DONE + t]);
         committed_o[t] = j;
@@ -294,28 +290,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int j = 0; ok && j < n; ++j) {
         const int vi = 2 * j + 1, ki = 2 * j + 2;
-        if (!(ok = wait(B_KV_FULL + vi % kSlots, (uint32_t)(vi / kSlots) & 1u))) break;
+        if (!(ok = wait(B_KV_FULL + vi % L::kSlots, (uint32_t)(vi / L::kSlots) & 1u))) break;
         if (j == n - 1 && tail_zero && !(ok = wait(B_VZ_READY, 0))) break;
         if (j < nA) {
           if (!(ok = wait(B_P_FULL + 0, (uint32_t)j & 1u))) break;
           issue_pv(0, j);
         }
-        if (j + 1 < n && !(ok = wait(B_KV_FULL + ki % kSlots, (uint32_t)(ki / kSlots) & 1u)))
+        if (j + 1 < n && !(ok = wait(B_KV_FULL + ki % L::kSlots, (uint32_t)(ki / L::kSlots) & 1u)))
           break;
-        if (j + 1 < nA) {
-          if (!(ok = wait(B_S_FREE + 0, (uint32_t)j & 1u))) break;
-          issue_s(0, j + 1);
-        }
+        if (j + 1 < nA) issue_s(0, j + 1);  // after PV_A(j) in issue order
         if (j < nB) {
           if (!(ok = wait(B_P_FULL + 1, (uint32_t)j & 1u))) break;
           issue_pv(1, j);
         }
-        umma_commit(&bars[B_KV_EMPTY + vi % kSlots]);  // V_j free once both PVs finish
-        if (j + 1 < nB) {
-          if (!(ok = wait(B_S_FREE + 1, (uint32_t)j & 1u))) break;
-          issue_s(1, j + 1);
-        }
-        if (j + 1 < n) umma_commit(&bars[B_KV_EMPTY + ki % kSlots]);  // K_j+1 after its S MMAs
+        umma_commit(&bars[B_KV_EMPTY + vi % L::kSlots]);  // V_j free once both PVs finish
+        if (j + 1 < nB) issue_s(1, j + 1);  // after PV_B(j) in issue order
+        if (j + 1 < n) umma_commit(&bars[B_KV_EMPTY + ki % L::kSlots]);  // K_j+1 after its S MMAs
       }
       // let the tensor core finish what was issued before the CTA exits
       for (int t = 0; t < 2; ++t)
@@ -336,7 +326,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int first_vis = it.s0 + it.i0 + t * BM;  // last key visible to the tile's row 0
     const int vis_last = first_vis + r;            // ... to this row
     const float c = p.scale_log2;
-    uint8_t* prow = sp + r * 128;
     float m = -INFINITY, l = 0.f;  // running max (raw score units), running sum
     bool ok = true;
     for (int j = 0; j < n_t; ++j) {
@@ -347,9 +336,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t s[128];
       tmem_ld128(s_col, s);
       tmem_ld_wait128(s);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_S_FREE + t]);
 
       const int key0 = j * BN;
       if (key0 + BN - 1 > first_vis) {  // tile straddles the causal frontier
@@ -394,26 +380,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         sum[(e >> 1) & 3] += e0 + e1;
         pk[e >> 1] = pack_bf16x2(e0, e1);
       }
-      // the P buffer (and O_t) are free once the previous PV in MMA order is done:
-      // for A(j) that is PV_B(j-1) (or PV_A(j-1) without B), for B(j) it is
-      // PV_A(j) (or PV_B(j-1) once A has no tile j)
-      int wb = -1;
-      uint32_t wpar = 0;
-      if (t == 0) {
-        if (j > 0) {
-          if (j - 1 < nB) { wb = B_O_DONE + 1; wpar = (uint32_t)(j - 1) & 1u; }
-          else { wb = B_O_DONE + 0; wpar = (uint32_t)(j - 1) & 1u; }
-        }
-      } else {
-        if (j < nA) { wb = B_O_DONE + 0; wpar = (uint32_t)j & 1u; }
-        else if (j > 0) { wb = B_O_DONE + 1; wpar = (uint32_t)(j - 1) & 1u; }
-      }
-      if (wb >= 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars[wb], wpar, abort_flag, p.status));
+      // O_t may be touched once its previous PV has completed
+      if (j > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + t], (uint32_t)(j - 1) & 1u,
+                                               abort_flag, p.status));
         if (!ok) break;
       }
+      tc_fence_after();
       if (__any_sync(0xffffffffu, need)) {
-        tc_fence_after();
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
@@ -423,16 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
           tmem_st32(o_col + cc * 32, o);
         }
-        tmem_st_wait();
       }
-#pragma unroll
-      for (int ch = 0; ch < BN / 8; ++ch) {
-        const int half = ch >> 3, c8 = ch & 7;
-        *reinterpret_cast<uint4*>(prow + half * L::kHalfBytes + ((c8 ^ (r & 7)) << 4)) =
-            make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-      }
+      // P (bf16 pairs) over the first 64 columns of the row's scores
+      tmem_st32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_st_wait();
       l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_P_FULL + t]);
