@@ -334,6 +334,12 @@ def run_gpu(args):
         plan.forward(q, kc, vc, bt_dev, out, lse, events=stage_events)
         plan.close()
 
+    def kernel_pass(stage_events):
+        # the same launches with per-stage events (stages back to back)
+        plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=ws)
+        plan.forward(q, kc, vc, bt_dev, out, lse, events=stage_events)
+        plan.close()
+
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -365,7 +371,7 @@ def run_gpu(args):
     for i in range(K):
         flush.zero_()
         ev[i][0].record(stream)
-        step(sev[i])
+        step()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -377,6 +383,12 @@ def run_gpu(args):
         step()
         torch.cuda.synchronize()
     clk = clocks.stop()
+    # per-kernel durations for the roofline: the same launches again, each
+    # stage bracketed by its own events (L2 flushed before every pass)
+    for i in range(K):
+        flush.zero_()
+        kernel_pass(sev[i])
+    torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     stage_ms = {}
     for si, name in enumerate(STAGES):

@@ -91,41 +91,14 @@ mb_status_t mb_attn_forward_timed(const mb_plan_t* plan, const void* q, const vo
   };
   cudaError_t e = cudaSuccess;
 
-  if (d.n_decode_items > 0) {
-    DecodeArgs a;
-    a.items = reinterpret_cast<const DecodeItem*>(ws + d.off_decode_items);
-    a.rows = reinterpret_cast<const RowDesc*>(ws + d.off_rows);
-    a.n_items = d.n_decode_items;
-    a.q = q;
-    a.k_cache = k_cache;
-    a.v_cache = v_cache;
-    a.block_table = block_table_dev;
-    a.max_blocks = d.max_blocks;
-    a.n_q_heads = d.n_q_heads;
-    a.n_kv_heads = d.n_kv_heads;
-    a.head_dim = d.head_dim;
-    a.page_size = d.page_size;
-    a.num_pages = d.num_pages;
-    a.scale_log2 = scale_log2;
-    a.out = out;
-    a.lse = lse;
-    a.part_o = reinterpret_cast<float*>(ws + d.off_part_o);
-    a.part_lse = reinterpret_cast<float*>(ws + d.off_part_lse);
-    a.status = status;
-    rec(MB_STAGE_DECODE, 0);
-    e = launch_decode(a, stream);
-    rec(MB_STAGE_DECODE, 1);
-    if (e != cudaSuccess) return MB_ERR_CUDA;
-  }
-  if (d.n_combine > 0) {
-    rec(MB_STAGE_COMBINE, 0);
-    e = launch_combine(reinterpret_cast<const CombineEntry*>(ws + d.off_combine), d.n_combine,
-                       reinterpret_cast<const float*>(ws + d.off_part_o),
-                       reinterpret_cast<const float*>(ws + d.off_part_lse), d.head_dim,
-                       d.n_q_heads, out, lse, stream);
-    rec(MB_STAGE_COMBINE, 1);
-    if (e != cudaSuccess) return MB_ERR_CUDA;
-  }
+  // With both kinds of work the prefill kernel goes first and the split-KV
+  // kernel is launched to overlap it (programmatic stream serialization):
+  // it starts once every prefill CTA has been dispatched and fills the SMs
+  // the prefill's heaviest-first queue leaves idle at its end. The combine
+  // kernel is ordered after both.
+  // (The timed variant launches back to back so that each stage's events
+  // bracket that stage alone.)
+  const bool overlap = d.n_prefill_items > 0 && d.n_decode_items > 0 && events == nullptr;
   if (d.n_prefill_items > 0) {
     CUtensorMap qm, km, vm;
     const cuuint64_t qdims[3] = {(cuuint64_t)d.head_dim, (cuuint64_t)d.n_q_heads,
@@ -160,6 +133,41 @@ mb_status_t mb_attn_forward_timed(const mb_plan_t* plan, const void* q, const vo
     rec(MB_STAGE_PREFILL, 0);
     e = launch_prefill(a, stream);
     rec(MB_STAGE_PREFILL, 1);
+    if (e != cudaSuccess) return MB_ERR_CUDA;
+  }
+  if (d.n_decode_items > 0) {
+    DecodeArgs a;
+    a.items = reinterpret_cast<const DecodeItem*>(ws + d.off_decode_items);
+    a.rows = reinterpret_cast<const RowDesc*>(ws + d.off_rows);
+    a.n_items = d.n_decode_items;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_table = block_table_dev;
+    a.max_blocks = d.max_blocks;
+    a.n_q_heads = d.n_q_heads;
+    a.n_kv_heads = d.n_kv_heads;
+    a.head_dim = d.head_dim;
+    a.page_size = d.page_size;
+    a.num_pages = d.num_pages;
+    a.scale_log2 = scale_log2;
+    a.out = out;
+    a.lse = lse;
+    a.part_o = reinterpret_cast<float*>(ws + d.off_part_o);
+    a.part_lse = reinterpret_cast<float*>(ws + d.off_part_lse);
+    a.status = status;
+    rec(MB_STAGE_DECODE, 0);
+    e = launch_decode(a, stream, overlap);
+    rec(MB_STAGE_DECODE, 1);
+    if (e != cudaSuccess) return MB_ERR_CUDA;
+  }
+  if (d.n_combine > 0) {
+    rec(MB_STAGE_COMBINE, 0);
+    e = launch_combine(reinterpret_cast<const CombineEntry*>(ws + d.off_combine), d.n_combine,
+                       reinterpret_cast<const float*>(ws + d.off_part_o),
+                       reinterpret_cast<const float*>(ws + d.off_part_lse), d.head_dim,
+                       d.n_q_heads, out, lse, stream);
+    rec(MB_STAGE_COMBINE, 1);
     if (e != cudaSuccess) return MB_ERR_CUDA;
   }
   return MB_OK;

@@ -234,14 +234,21 @@ __global__ void __launch_bounds__(kWarps * 32) splitkv_kernel(const DecodeArgs a
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, bool overlap_previous) {
   if (a.n_items <= 0) return cudaSuccess;
   const int ps_shift = __builtin_ctz((unsigned)a.page_size);
-  if (a.head_dim == 128)
-    splitkv_kernel<128><<<a.n_items, kWarps * 32, 0, s>>>(a, ps_shift);
-  else
-    splitkv_kernel<64><<<a.n_items, kWarps * 32, 0, s>>>(a, ps_shift);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.n_items);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_previous ? 1 : 0;
+  if (a.head_dim == 128) return cudaLaunchKernelEx(&cfg, splitkv_kernel<128>, a, ps_shift);
+  return cudaLaunchKernelEx(&cfg, splitkv_kernel<64>, a, ps_shift);
 }
 
 }  // namespace mb

@@ -32,7 +32,10 @@ struct DecodeArgs {
   float* part_lse;   // log2 domain
   int32_t* status;
 };
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+// overlap_previous: launch with programmatic stream serialization, so the
+// kernel may start while the previous kernel on the stream (which must not
+// produce anything it reads) is still running.
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, bool overlap_previous = false);
 
 // LSE merge of partials (combine.cu).
 cudaError_t launch_combine(const CombineEntry* entries, int32_t n, const float* part_o,

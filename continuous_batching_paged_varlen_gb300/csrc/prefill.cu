@@ -125,6 +125,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
 
+  // a kernel launched after this one with programmatic stream serialization
+  // (the split-KV kernel of the same iteration) may start once every CTA of
+  // this grid has been dispatched; it reads nothing this kernel writes
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   const PrefillItem it = p.items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows_a = min(BM, it.n_rows);

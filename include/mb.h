@@ -192,15 +192,20 @@ mb_status_t mb_attn_plan_ex(const mb_request_t* reqs, int32_t n_reqs,
  * request covers are not written), lse [total_q, Hq] fp32 natural-log
  * log-sum-exp of the scaled visible scores (nullable). No device->host
  * traffic and no allocation: the launch sequence can be captured in a CUDA
- * graph. Device-detected errors go to the workspace status word. */
+ * graph. When the plan holds both prefill and split-KV work, the prefill
+ * kernel is launched first and the split-KV kernel overlaps its end
+ * (programmatic dependent launch on the same stream); everything is ordered
+ * on `stream` as usual. Device-detected errors go to the workspace status
+ * word. */
 mb_status_t mb_attn_forward(const mb_plan_t* plan, const void* q,
                             const void* k_cache, const void* v_cache,
                             const int32_t* block_table_dev, void* out,
                             float* lse, cudaStream_t stream);
 
 /* mb_attn_forward that also records events[2*s] / events[2*s+1] on stream
- * around stage s (MB_STAGE_*) when that stage launches. events: array of
- * 2 * MB_NUM_STAGES created events (entries may be NULL). */
+ * around stage s (MB_STAGE_*) when that stage launches. Stages are launched
+ * back to back (no overlap) so each pair brackets its stage alone. events:
+ * array of 2 * MB_NUM_STAGES created events (entries may be NULL). */
 mb_status_t mb_attn_forward_timed(const mb_plan_t* plan, const void* q,
                                   const void* k_cache, const void* v_cache,
                                   const int32_t* block_table_dev, void* out,
