@@ -91,6 +91,17 @@ mb_status_t mb_attn_forward_timed(const mb_plan_t* plan, const void* q, const vo
   };
   cudaError_t e = cudaSuccess;
 
+  // K/V tensor maps (both attention kernels stage pages with TMA)
+  CUtensorMap qm, km, vm;
+  {
+    const cuuint64_t kvdims[2] = {(cuuint64_t)d.head_dim,
+                                  (cuuint64_t)d.num_pages * d.n_kv_heads * d.page_size};
+    const cuuint64_t kvstr[1] = {(cuuint64_t)d.head_dim * 2};
+    const cuuint32_t kvbox[2] = {64, (cuuint32_t)d.page_size};
+    if (!make_map(&km, k_cache, 2, kvdims, kvstr, kvbox) ||
+        !make_map(&vm, v_cache, 2, kvdims, kvstr, kvbox))
+      return MB_ERR_CUDA;
+  }
   // With both kinds of work the prefill kernel goes first and the split-KV
   // kernel is launched to overlap it (programmatic stream serialization):
   // it starts once every prefill CTA has been dispatched and fills the SMs
@@ -100,19 +111,12 @@ mb_status_t mb_attn_forward_timed(const mb_plan_t* plan, const void* q, const vo
   // bracket that stage alone.)
   const bool overlap = d.n_prefill_items > 0 && d.n_decode_items > 0 && events == nullptr;
   if (d.n_prefill_items > 0) {
-    CUtensorMap qm, km, vm;
     const cuuint64_t qdims[3] = {(cuuint64_t)d.head_dim, (cuuint64_t)d.n_q_heads,
                                  (cuuint64_t)d.total_q};
     const cuuint64_t qstr[2] = {(cuuint64_t)d.head_dim * 2,
                                 (cuuint64_t)d.n_q_heads * d.head_dim * 2};
     const cuuint32_t qbox[3] = {64, 1, (cuuint32_t)kPrefillTileM};
-    const cuuint64_t kvdims[2] = {(cuuint64_t)d.head_dim,
-                                  (cuuint64_t)d.num_pages * d.n_kv_heads * d.page_size};
-    const cuuint64_t kvstr[1] = {(cuuint64_t)d.head_dim * 2};
-    const cuuint32_t kvbox[2] = {64, (cuuint32_t)d.page_size};
-    if (!make_map(&qm, q, 3, qdims, qstr, qbox) || !make_map(&km, k_cache, 2, kvdims, kvstr, kvbox) ||
-        !make_map(&vm, v_cache, 2, kvdims, kvstr, kvbox))
-      return MB_ERR_CUDA;
+    if (!make_map(&qm, q, 3, qdims, qstr, qbox)) return MB_ERR_CUDA;
     PrefillArgs a;
     a.items = reinterpret_cast<const PrefillItem*>(ws + d.off_prefill_items);
     a.n_items = d.n_prefill_items;
@@ -156,6 +160,8 @@ mb_status_t mb_attn_forward_timed(const mb_plan_t* plan, const void* q, const vo
     a.part_o = reinterpret_cast<float*>(ws + d.off_part_o);
     a.part_lse = reinterpret_cast<float*>(ws + d.off_part_lse);
     a.status = status;
+    a.k_map = &km;
+    a.v_map = &vm;
     rec(MB_STAGE_DECODE, 0);
     e = launch_decode(a, stream, overlap);
     rec(MB_STAGE_DECODE, 1);

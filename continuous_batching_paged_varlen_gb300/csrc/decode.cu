@@ -1,28 +1,35 @@
 // Split-KV attention for rows with few new queries (decode steps, small
 // chunks) and for shared-prefix cascade groups.
 //
-// One CTA owns up to 8 query rows that all read the same KV head -- the g
+// One CTA owns up to 128 query rows that all read the same KV head -- the g
 // query heads of a GQA group ("How To Scale Your Model notes (7-8)",
-// section 3: g queries share one KV head, so KV bytes are read once for all
-// g of them) and, for a cascade group, the rows of every request that shares
-// the prefix pages ("How To Scale Your Model notes (7-8)", section 3: load a
-// common KV block once, apply it to all the requests' queries, keep each
-// request's own softmax state). The CTA walks the key range [k_begin, k_end)
-// of one block-table row and keeps an online softmax (running max m, running
-// sum l, accumulator) per row. Each key is masked by the row's own
-// visibility bound (S0 + i + 1, "How To Scale Your Model notes (7-8)",
-// section 2), so decode rows (m = 1) see everything and multi-row requests
-// get the causal diagonal block.
+// section 3: g queries share one KV head, so its K/V bytes are read once for
+// all g of them) and, for a cascade group, the rows of every request whose
+// block tables share the prefix pages ("How To Scale Your Model notes
+// (7-8)", section 3: load a common KV block once, apply it to every sharing
+// request's queries, each request keeping its own softmax state). The CTA
+// walks the key range [k_begin, k_end) of one block-table row in 128-key
+// tiles and keeps, per row, a running max, a running sum and the output
+// accumulator; each key is masked by the row's own visibility bound
+// (S0 + i + 1, "How To Scale Your Model notes (7-8)", section 2). The result
+// is the final row (bf16 out + LSE) or, when the key range was split, a
+// normalised partial (fp32 O, log2-domain LSE) for the combine kernel.
 //
-// The result is either the final row (bf16 out + LSE) or, when the key
-// range was split, a normalised partial (fp32 O, log2-domain LSE) that the
-// combine kernel merges.
-//
-// Work split inside the CTA: 4 warps take interleaved 32-key blocks; in a
-// block lane = key for the q.k products (q rows live in shared memory as
-// fp32 pre-scaled by scale * log2 e, K rows are read straight from the
-// page), then lane = 4 (or 2) consecutive head dims for p.V. The four warps'
-// (m, l, acc) are merged through shared memory at the end.
+// This path is bound by HBM bandwidth, so the design spends everything on
+// keeping bytes in flight and almost nothing on issue slots:
+//   warp 4      TMA producer: K_j, V_j, K_j+1, ... page by page through the
+//               block table into a 6-slot ring (one box per page and 64-column
+//               block, one lane per box), 128-byte swizzle.
+//   warp 5      TMEM allocation; one lane issues S = Q K^T (M 128 = the
+//               gathered rows, N 128 keys, K = D) into a double-buffered TMEM
+//               tile and O += P V (P from TMEM, V from shared memory). The
+//               tensor core is mostly idle: it only spares the CUDA cores.
+//   warps 0-3   one thread per query row; only warps that own real rows run:
+//               TMEM load of the row's 128 scores, mask, online max / sum in
+//               the log2 domain, P back into TMEM over the scores, rare O
+//               rescale, epilogue.
+// Every wait is bounded; on a timeout the CTA raises its abort flag, drains
+// what it issued, frees its TMEM and returns.
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -33,202 +40,359 @@
 namespace mb {
 namespace {
 
-constexpr int kR = kRowsPerDecodeItem;
-constexpr int kWarps = 4;
-constexpr float kLn2 = 0.6931471805599453f;
+using namespace dev;
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
+constexpr int BM = 128;  // gathered query rows (TMEM lanes)
+constexpr int BN = 128;  // keys per tile
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;    // + 128 * buffer
+constexpr uint32_t kColO = 256;
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint64_t kDrainNs = 200000000ull;
+
+enum {
+  kSlots = 6,
+  B_KV_FULL = 0,              // + slot
+  B_KV_EMPTY = kSlots,        // + slot
+  B_S_FULL = 2 * kSlots,      // + buffer
+  B_P_FULL = 2 * kSlots + 2,
+  B_O_DONE = 2 * kSlots + 3,
+  B_VZ_READY = 2 * kSlots + 4,
+  B_COUNT = 2 * kSlots + 5
+};
 
 template <int D>
-__global__ void __launch_bounds__(kWarps * 32) splitkv_kernel(const DecodeArgs a,
-                                                              const int ps_shift) {
-  constexpr int DL = D / 32;  // head dims per lane in the p.V phase
-  __shared__ __align__(16) float q_s[kR][D];
-  __shared__ float m_s[kWarps][kR];
-  __shared__ float l_s[kWarps][kR];
-  __shared__ __align__(16) float acc_s[kWarps][kR][D];
-  __shared__ RowDesc rd[kR];
+struct Layout {
+  static constexpr int kHalves = D / 64;
+  static constexpr uint32_t kHalfBytes = 128 * 128;
+  static constexpr uint32_t kTileBytes = kHalves * kHalfBytes;
+  static constexpr uint32_t q_off = 0;
+  static constexpr uint32_t kv_off = kTileBytes;
+  static constexpr uint32_t bar_off = kv_off + kSlots * kTileBytes;
+  static constexpr uint32_t misc_off = bar_off + B_COUNT * 8;
+  static constexpr uint32_t kBytes = misc_off + 16;
+  // + alignment slack; more than half the SM so that one CTA holds the SM's
+  // 512 TMEM columns alone
+  static constexpr uint32_t kAlloc =
+      (kBytes + 1024 > 232448u / 2 + 1024) ? kBytes + 1024 : 232448u / 2 + 1024;
+  static_assert(kAlloc <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    splitkv_kernel(const DecodeArgs a, const int ps_shift,
+                   const __grid_constant__ CUtensorMap k_map,
+                   const __grid_constant__ CUtensorMap v_map) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sq = smem + L::q_off;
+  uint8_t* skv = smem + L::kv_off;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar_off);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
 
   const DecodeItem it = a.items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nr = it.n_rows;
-  if (threadIdx.x < kR) {
-    RowDesc d;
-    d.q_index = 0;
-    d.q_head = 0;
-    d.vis_end = 0;  // unused rows see nothing
-    d.dst = -1;
-    if ((int)threadIdx.x < nr) d = a.rows[it.row_begin + threadIdx.x];
-    rd[threadIdx.x] = d;
+  const int n = ceil_div(it.k_end - it.k_begin, BN);
+  const bool tail_zero = it.k_begin + n * BN > it.k_end;
+  const int active_warps = ceil_div(nr, 32);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&bars[B_KV_FULL + s], 1);
+      mbar_init(&bars[B_KV_EMPTY + s], 1);
+    }
+    mbar_init(&bars[B_S_FULL + 0], 1);
+    mbar_init(&bars[B_S_FULL + 1], 1);
+    mbar_init(&bars[B_P_FULL], active_warps);
+    mbar_init(&bars[B_O_DONE], 1);
+    mbar_init(&bars[B_VZ_READY], 1);
+    *abort_flag = 0;
+    fence_barrier_init();
   }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  // gather the item's query rows into the K-major 128-byte-swizzled Q tile
+  // (rows past n_rows are zero)
+  {
+    const uint4* q = static_cast<const uint4*>(a.q);
+    constexpr int CH = D / 8;  // 16-byte chunks per row
+    for (int idx = threadIdx.x; idx < BM * CH; idx += kThreads) {
+      const int r = idx / CH, c = idx - r * CH;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (r < nr) {
+        const RowDesc rd = a.rows[it.row_begin + r];
+        v = __ldg(q + ((int64_t)rd.q_index * a.n_q_heads + rd.q_head) * CH + c);
+      }
+      const int half = c >> 3, c8 = c & 7;
+      *reinterpret_cast<uint4*>(sq + half * L::kHalfBytes + r * 128 + ((c8 ^ (r & 7)) << 4)) = v;
+    }
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
   __syncthreads();
-  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-  for (int i = threadIdx.x; i < kR * D; i += kWarps * 32) {
-    const int r = i / D, d = i - r * D;
-    float v = 0.f;
-    if (r < nr)
-      v = __bfloat162float(q[((int64_t)rd[r].q_index * a.n_q_heads + rd[r].q_head) * D + d]) *
-          a.scale_log2;
-    q_s[r][d] = v;
-  }
-  int vis[kR];
-#pragma unroll
-  for (int r = 0; r < kR; ++r) vis[r] = rd[r].vis_end;
-  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
 
-  float m[kR], l[kR], acc[kR][DL];
-#pragma unroll
-  for (int r = 0; r < kR; ++r) {
-    m[r] = -INFINITY;
-    l[r] = 0.f;
-#pragma unroll
-    for (int e = 0; e < DL; ++e) acc[r][e] = 0.f;
-  }
-
-  const int32_t* btrow = a.block_table + (int64_t)it.bt_row * a.max_blocks;
-  const int ps_mask = (1 << ps_shift) - 1;
-  const uint4* kc = static_cast<const uint4*>(a.k_cache);
-  const __nv_bfloat16* vc = static_cast<const __nv_bfloat16*>(a.v_cache);
-
-  for (int kb = it.k_begin + warp * 32; kb < it.k_end; kb += 32 * kWarps) {
-    const int j = kb + lane;
-    int valid = j < it.k_end;
-    int64_t rowidx = 0;
-    if (valid) {
-      const int page = __ldg(btrow + (j >> ps_shift));
-      if ((unsigned)page >= (unsigned)a.num_pages) {
-        dev::set_status(a.status, MB_ERR_DEVICE_INDEX);
-        valid = 0;
-      } else {
-        rowidx = (((int64_t)page * a.n_kv_heads + it.kv_head) << ps_shift) + (j & ps_mask);
-      }
-    }
-    // ---- scores of this lane's key against every row
-    float s[kR];
-#pragma unroll
-    for (int r = 0; r < kR; ++r) s[r] = 0.f;
-    if (valid) {
-      const uint4* kp = kc + rowidx * (D / 8);
-      uint4 kr[D / 8];
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) kr[c] = __ldg(kp + c);
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const float k0 = dev::bf16_lo(kr[c].x), k1 = dev::bf16_hi(kr[c].x);
-        const float k2 = dev::bf16_lo(kr[c].y), k3 = dev::bf16_hi(kr[c].y);
-        const float k4 = dev::bf16_lo(kr[c].z), k5 = dev::bf16_hi(kr[c].z);
-        const float k6 = dev::bf16_lo(kr[c].w), k7 = dev::bf16_hi(kr[c].w);
-#pragma unroll
-        for (int r = 0; r < kR; ++r) {
-          const float4 qa = *reinterpret_cast<const float4*>(&q_s[r][c * 8]);
-          const float4 qb = *reinterpret_cast<const float4*>(&q_s[r][c * 8 + 4]);
-          s[r] = fmaf(qa.x, k0, s[r]);
-          s[r] = fmaf(qa.y, k1, s[r]);
-          s[r] = fmaf(qa.z, k2, s[r]);
-          s[r] = fmaf(qa.w, k3, s[r]);
-          s[r] = fmaf(qb.x, k4, s[r]);
-          s[r] = fmaf(qb.y, k5, s[r]);
-          s[r] = fmaf(qb.z, k6, s[r]);
-          s[r] = fmaf(qb.w, k7, s[r]);
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    const int ps = 1 << ps_shift;
+    const int npg = BN / ps, nbox = npg * L::kHalves;
+    const int my_pg = lane % npg, my_h2 = lane / npg;
+    const int32_t* btrow = a.block_table + (int64_t)it.bt_row * a.max_blocks;
+    const int last_block = (it.k_end - 1) >> ps_shift;
+    const int first_block = it.k_begin >> ps_shift;  // k_begin is page-aligned
+    int32_t my_y = 0;
+    int issued = 0;
+    for (int i = 0; i < 2 * n; ++i) {
+      const int j = i >> 1, slot = i % kSlots;
+      const uint32_t ph = (uint32_t)(i / kSlots) & 1u;
+      if (i >= kSlots &&
+          !__all_sync(0xffffffffu, mbar_wait(&bars[B_KV_EMPTY + slot], ph ^ 1u, abort_flag,
+                                             a.status)))
+        break;
+      if ((i & 1) == 0 && lane < npg) {
+        int b = first_block + j * npg + lane;
+        if (b > last_block) b = last_block;  // keys past k_end: masked, V zeroed
+        int32_t page = __ldg(btrow + b);
+        if ((unsigned)page >= (unsigned)a.num_pages) {
+          set_status(a.status, MB_ERR_DEVICE_INDEX);
+          page = 0;
         }
+        my_y = (page * a.n_kv_heads + it.kv_head) << ps_shift;
       }
+      const int32_t y = __shfl_sync(0xffffffffu, my_y, my_pg);
+      if (lane == 0) mbar_arrive_expect_tx(&bars[B_KV_FULL + slot], L::kTileBytes);
+      __syncwarp();
+      if (lane < nbox)
+        tma_load_2d(skv + slot * L::kTileBytes + my_h2 * L::kHalfBytes + my_pg * ps * 128,
+                    (i & 1) ? &v_map : &k_map, &bars[B_KV_FULL + slot], my_h2 * 64, y);
+      issued = i + 1;
     }
-    // ---- online softmax update (m is warp-uniform, l is kept per lane)
-    float p[kR];
-#pragma unroll
-    for (int r = 0; r < kR; ++r) {
-      const float sr = (valid && j < vis[r]) ? s[r] : -INFINITY;
-      const float mn = fmaxf(m[r], warp_max(sr));
-      if (mn == -INFINITY) {  // nothing visible to this row yet
-        p[r] = 0.f;
-        continue;
-      }
-      const float alpha = dev::fast_exp2(m[r] - mn);
-      p[r] = dev::fast_exp2(sr - mn);
-      l[r] = l[r] * alpha + p[r];
-#pragma unroll
-      for (int e = 0; e < DL; ++e) acc[r][e] *= alpha;
-      m[r] = mn;
-    }
-    // ---- p . V, lanes over head dims
-    const int nk = min(32, it.k_end - kb);
-#pragma unroll 4
-    for (int jj = 0; jj < nk; ++jj) {
-      const int64_t vr = __shfl_sync(0xffffffffu, rowidx, jj);
-      const int vv = __shfl_sync(0xffffffffu, valid, jj);
-      float vf[DL];
-      if (vv) {
-        if constexpr (DL == 4) {
-          const uint2 u = __ldg(reinterpret_cast<const uint2*>(vc + vr * D) + lane);
-          vf[0] = dev::bf16_lo(u.x);
-          vf[1] = dev::bf16_hi(u.x);
-          vf[2] = dev::bf16_lo(u.y);
-          vf[3] = dev::bf16_hi(u.y);
-        } else {
-          const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(vc + vr * D) + lane);
-          vf[0] = dev::bf16_lo(u);
-          vf[1] = dev::bf16_hi(u);
+    __syncwarp();
+    if (tail_zero && issued == 2 * n) {
+      // keys >= k_end in the last V tile: zero their rows (P is 0 there, and
+      // an unwritten slot may hold a non-finite value)
+      const int i = 2 * n - 1, slot = i % kSlots;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_KV_FULL + slot],
+                                                        (uint32_t)(i / kSlots) & 1u, abort_flag,
+                                                        a.status));
+      if (ok) {
+        const int r0 = it.k_end - (it.k_begin + (n - 1) * BN);
+        const int nz = BN - r0;
+        uint8_t* vb = skv + slot * L::kTileBytes;
+        for (int idx = lane; idx < nz * L::kHalves * 8; idx += 32) {
+          const int c = idx & 7;
+          const int rr = idx >> 3;
+          const int h2 = rr / nz;
+          const int row = r0 + (rr - h2 * nz);
+          *reinterpret_cast<uint4*>(vb + h2 * L::kHalfBytes + row * 128 + c * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
         }
-      } else {
-#pragma unroll
-        for (int e = 0; e < DL; ++e) vf[e] = 0.f;
+        fence_proxy_async_smem();
       }
-#pragma unroll
-      for (int r = 0; r < kR; ++r) {
-        const float pj = __shfl_sync(0xffffffffu, p[r], jj);
-#pragma unroll
-        for (int e = 0; e < DL; ++e) acc[r][e] = fmaf(pj, vf[e], acc[r][e]);
-      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_VZ_READY]);
     }
-  }
-
-  // ---- merge the four warps
-#pragma unroll
-  for (int r = 0; r < kR; ++r) {
-    const float lr = warp_sum(l[r]);
+    if (lane == 0)
+      for (int i = max(0, issued - kSlots); i < issued; ++i)
+        mbar_drain(&bars[B_KV_FULL + i % kSlots], (uint32_t)(i / kSlots) & 1u, kDrainNs);
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      m_s[warp][r] = m[r];
-      l_s[warp][r] = lr;
-    }
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
+      const uint32_t qa = smem_u32(sq);
+      const uint32_t kva = smem_u32(skv);
+      int last_pv = -1;
+      auto wait = [&](int b, uint32_t parity) -> bool {
+        const bool ok = mbar_wait(&bars[b], parity, abort_flag, a.status);
+        tc_fence_after();
+        return ok;
+      };
+      auto issue_s = [&](int j) -> bool {
+        const int ki = 2 * j;
+        if (!wait(B_KV_FULL + ki % kSlots, (uint32_t)(ki / kSlots) & 1u)) return false;
+        const uint32_t k0 = kva + (ki % kSlots) * L::kTileBytes;
 #pragma unroll
-    for (int e = 0; e < DL; ++e) acc_s[warp][r][lane * DL + e] = acc[r][e];
-  }
-  __syncthreads();
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-  for (int i = threadIdx.x; i < nr * D; i += kWarps * 32) {
-    const int r = i / D, d = i - r * D;
-    float M = -INFINITY;
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
+          umma_bf16_ss(tmem + kColS + 128 * (j & 1), sdesc_sw128(qa + off, 16, 1024),
+                       sdesc_sw128(k0 + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars[B_S_FULL + (j & 1)]);
+        umma_commit(&bars[B_KV_EMPTY + ki % kSlots]);
+        return true;
+      };
+      bool ok = n > 0 && issue_s(0);
+      if (ok && n > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < n; ++j) {
+        const int vi = 2 * j + 1;
+        if (!(ok = wait(B_KV_FULL + vi % kSlots, (uint32_t)(vi / kSlots) & 1u))) break;
+        if (j == n - 1 && tail_zero && !(ok = wait(B_VZ_READY, 0))) break;
+        if (!(ok = wait(B_P_FULL, (uint32_t)j & 1u))) break;
+        const uint32_t v0 = kva + (vi % kSlots) * L::kTileBytes;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, m_s[w][r]);
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float f = dev::fast_exp2(m_s[w][r] - M);
-        L = fmaf(l_s[w][r], f, L);
-        O = fmaf(acc_s[w][r][d], f, O);
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t bd = sdesc_sw128(v0 + kk * 2048, L::kHalfBytes, 1024);
+          umma_bf16_ts(tmem + kColO, tmem + kColS + 128 * (j & 1) + kk * 8, bd, idesc_pv,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&bars[B_O_DONE]);
+        umma_commit(&bars[B_KV_EMPTY + vi % kSlots]);
+        last_pv = j;
+        // S(j+2) reuses this buffer; it follows PV(j) in issue order
+        if (j + 2 < n && !(ok = issue_s(j + 2))) break;
       }
+      if (last_pv >= 0) mbar_drain(&bars[B_O_DONE], (uint32_t)last_pv & 1u, kDrainNs);
     }
-    const float o = L > 0.f ? O / L : 0.f;
-    const float lse2 = L > 0.f ? M + log2f(L) : -INFINITY;
-    const RowDesc rw = rd[r];
-    if (rw.dst < 0) {
-      const int64_t orow = (int64_t)rw.q_index * a.n_q_heads + rw.q_head;
-      out[orow * D + d] = __float2bfloat16_rn(o);
-      if (d == 0 && a.lse) a.lse[orow] = lse2 * kLn2;
-    } else {
-      a.part_o[(int64_t)rw.dst * D + d] = o;
-      if (d == 0) a.part_lse[rw.dst] = lse2;
+  } else if (warp < active_warps) {
+    // ------------------------------------------------------------ softmax
+    const int r = warp * 32 + lane;
+    const bool valid = r < nr;
+    RowDesc rd;
+    rd.q_index = 0;
+    rd.q_head = 0;
+    rd.vis_end = 0;
+    rd.dst = -1;
+    if (valid) rd = a.rows[it.row_begin + r];
+    // visible keys of this row inside the item: [k_begin, min(k_end, vis_end))
+    const int vis_hi = min(it.k_end, rd.vis_end);
+    const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+    const uint32_t o_col = tmem + lane_addr + kColO;
+    const float c = a.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const uint32_t s_col = tmem + lane_addr + kColS + 128 * (j & 1);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_S_FULL + (j & 1)], (uint32_t)(j >> 1) & 1u,
+                                             abort_flag, a.status));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[128];
+      tmem_ld128(s_col, s);
+      tmem_ld_wait128(s);
+      const int lim = vis_hi - (it.k_begin + j * BN);  // keys e < lim are visible
+      if (lim < BN) {
+#pragma unroll
+        for (int e = 0; e < 128; ++e)
+          if (e >= lim) s[e] = __float_as_uint(-INFINITY);
+      }
+      float mx[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) mx[k] = __uint_as_float(s[k]);
+#pragma unroll
+      for (int e = 16; e < 128; e += 16)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(s[e + k]));
+#pragma unroll
+      for (int w2 = 8; w2 > 0; w2 >>= 1)
+#pragma unroll
+        for (int k = 0; k < w2; ++k) mx[k] = fmaxf(mx[k], mx[k + w2]);
+      const float m_new = fmaxf(m, mx[0]);
+      float alpha = 1.f;
+      bool need = false;
+      if (m == -INFINITY) {
+        m = m_new;  // nothing accumulated yet (O is written with accumulate off or all-zero P)
+      } else if ((m_new - m) * c > kRescaleThreshold) {
+        need = true;
+        alpha = fast_exp2((m - m_new) * c);
+        l *= alpha;
+        m = m_new;
+      }
+      const float mc = (m == -INFINITY) ? 0.f : m * c;
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[64];
+#pragma unroll
+      for (int e = 0; e < 128; e += 2) {
+        const float e0 = fast_exp2(fmaf(__uint_as_float(s[e]), c, -mc));
+        const float e1 = fast_exp2(fmaf(__uint_as_float(s[e + 1]), c, -mc));
+        sum[(e >> 1) & 3] += e0 + e1;
+        pk[e >> 1] = pack_bf16x2(e0, e1);
+      }
+      l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+      if (j > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE], (uint32_t)(j - 1) & 1u,
+                                               abort_flag, a.status));
+        if (!ok) break;
+      }
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(o_col + cc * 32, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(o_col + cc * 32, o);
+        }
+      }
+      tmem_st32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_P_FULL]);
     }
+    if (ok && n > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE], (uint32_t)(n - 1) & 1u,
+                                             abort_flag, a.status));
+    if (ok && n > 0) {
+      tc_fence_after();
+      const bool any = l > 0.f;
+      const float inv = any ? 1.f / l : 0.f;
+      const float lse2 = any ? m * c + log2f(l) : -INFINITY;
+      // the TMEM loads are warp-collective: every lane runs them, whatever
+      // its row; only the stores depend on the row
+      const bool final_row = rd.dst < 0;
+      const int64_t orow = (int64_t)rd.q_index * a.n_q_heads + rd.q_head;
+      uint4* dst_out =
+          reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * D);
+      float4* dst_part = reinterpret_cast<float4*>(a.part_o + (int64_t)max(rd.dst, 0) * D);
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(o_col + cc * 32, o);
+        tmem_ld_wait(o);
+        if (valid && final_row) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
+            dst_out[cc * 4 + q4] = v;
+          }
+        } else if (valid) {
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4)
+            dst_part[cc * 8 + q4] = make_float4(__uint_as_float(o[q4 * 4 + 0]) * inv,
+                                                __uint_as_float(o[q4 * 4 + 1]) * inv,
+                                                __uint_as_float(o[q4 * 4 + 2]) * inv,
+                                                __uint_as_float(o[q4 * 4 + 3]) * inv);
+        }
+      }
+      if (valid && final_row && a.lse) a.lse[orow] = lse2 * kLn2;
+      if (valid && !final_row) a.part_lse[rd.dst] = lse2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -239,16 +403,26 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, bool overlap_prev
   const int ps_shift = __builtin_ctz((unsigned)a.page_size);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.n_items);
-  cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = 0;
+  cfg.blockDim = dim3(kThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap_previous ? 1 : 0;
-  if (a.head_dim == 128) return cudaLaunchKernelEx(&cfg, splitkv_kernel<128>, a, ps_shift);
-  return cudaLaunchKernelEx(&cfg, splitkv_kernel<64>, a, ps_shift);
+  cudaError_t e;
+  if (a.head_dim == 128) {
+    cfg.dynamicSmemBytes = Layout<128>::kAlloc;
+    e = cudaFuncSetAttribute(splitkv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Layout<128>::kAlloc);
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, splitkv_kernel<128>, a, ps_shift, *a.k_map, *a.v_map);
+  }
+  cfg.dynamicSmemBytes = Layout<64>::kAlloc;
+  e = cudaFuncSetAttribute(splitkv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)Layout<64>::kAlloc);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, splitkv_kernel<64>, a, ps_shift, *a.k_map, *a.v_map);
 }
 
 }  // namespace mb

@@ -31,6 +31,8 @@ struct DecodeArgs {
   float* part_o;
   float* part_lse;   // log2 domain
   int32_t* status;
+  const CUtensorMap* k_map;  // host copies, passed by value to the kernel
+  const CUtensorMap* v_map;
 };
 // overlap_previous: launch with programmatic stream serialization, so the
 // kernel may start while the previous kernel on the stream (which must not

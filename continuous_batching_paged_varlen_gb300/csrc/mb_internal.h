@@ -20,7 +20,7 @@
 namespace mb {
 
 constexpr int kStatusBytes = 256;
-constexpr int kRowsPerDecodeItem = 8;   // query rows one split-KV CTA owns
+constexpr int kRowsPerDecodeItem = 128; // query rows one split-KV CTA owns (TMEM lanes)
 constexpr int kPrefillTileM = 128;      // query rows per prefill tile (one TMEM accumulator)
 constexpr int kPrefillTileN = 128;      // keys per prefill KV tile
 constexpr int kPrefillCtaRows = 256;    // query rows per prefill CTA (two tiles)

@@ -108,6 +108,16 @@ extern "C" mb_status_t mb_attn_forward_noalloc(const mb_plan_t* plan, const void
     return MB_ERR_CUDA;
 
   const float scale_log2 = d.scale * kLog2e;
+  CUtensorMap km, vm;
+  {
+    const cuuint64_t kvdims[2] = {(cuuint64_t)d.head_dim,
+                                  (cuuint64_t)d.num_pages * d.n_kv_heads * d.page_size};
+    const cuuint64_t kvstr[1] = {(cuuint64_t)d.head_dim * 2};
+    const cuuint32_t kvbox[2] = {64, (cuuint32_t)d.page_size};
+    if (!make_map(&km, k_cache, 2, kvdims, kvstr, kvbox) ||
+        !make_map(&vm, v_cache, 2, kvdims, kvstr, kvbox))
+      return MB_ERR_CUDA;
+  }
   if (d.n_decode_items > 0) {
     DecodeArgs a;
     a.items = reinterpret_cast<const DecodeItem*>(ws + d.off_decode_items);
@@ -129,6 +139,8 @@ extern "C" mb_status_t mb_attn_forward_noalloc(const mb_plan_t* plan, const void
     a.part_o = reinterpret_cast<float*>(ws + d.off_part_o);
     a.part_lse = reinterpret_cast<float*>(ws + d.off_part_lse);
     a.status = status;
+    a.k_map = &km;
+    a.v_map = &vm;
     if (launch_decode(a, stream) != cudaSuccess) return MB_ERR_CUDA;
   }
   if (d.n_combine > 0 &&
@@ -138,20 +150,13 @@ extern "C" mb_status_t mb_attn_forward_noalloc(const mb_plan_t* plan, const void
                      d.n_q_heads, out, lse, stream) != cudaSuccess)
     return MB_ERR_CUDA;
   if (d.n_prefill_items > 0) {
-    CUtensorMap qm, km, vm;
+    CUtensorMap qm;
     const cuuint64_t qdims[3] = {(cuuint64_t)d.head_dim, (cuuint64_t)d.n_q_heads,
                                  (cuuint64_t)d.total_q};
     const cuuint64_t qstr[2] = {(cuuint64_t)d.head_dim * 2,
                                 (cuuint64_t)d.n_q_heads * d.head_dim * 2};
     const cuuint32_t qbox[3] = {64, 1, (cuuint32_t)kPrefillTileM};
-    const cuuint64_t kvdims[2] = {(cuuint64_t)d.head_dim,
-                                  (cuuint64_t)d.num_pages * d.n_kv_heads * d.page_size};
-    const cuuint64_t kvstr[1] = {(cuuint64_t)d.head_dim * 2};
-    const cuuint32_t kvbox[2] = {64, (cuuint32_t)d.page_size};
-    if (!make_map(&qm, q, 3, qdims, qstr, qbox) ||
-        !make_map(&km, k_cache, 2, kvdims, kvstr, kvbox) ||
-        !make_map(&vm, v_cache, 2, kvdims, kvstr, kvbox))
-      return MB_ERR_CUDA;
+    if (!make_map(&qm, q, 3, qdims, qstr, qbox)) return MB_ERR_CUDA;
     PrefillArgs a;
     a.items = reinterpret_cast<const PrefillItem*>(ws + d.off_prefill_items);
     a.n_items = d.n_prefill_items;

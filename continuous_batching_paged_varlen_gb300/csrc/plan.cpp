@@ -24,8 +24,10 @@ using namespace mb;
 namespace {
 
 constexpr int kDefaultPrefillMinRows = 16;
-constexpr int kDefaultTargetCtas = 4 * 152;
-constexpr int kMinChunk = 256;
+// split-KV CTAs to aim for (one resident CTA per SM, ~2 waves on 152 SMs)
+constexpr int kDefaultTargetCtas = 2 * 152;
+// shortest automatic split-KV chunk: 8 key tiles amortise a CTA's set-up
+constexpr int kMinChunk = 1024;
 
 bool is_pow2_in(int v, int lo, int hi) {
   return v >= lo && v <= hi && (v & (v - 1)) == 0;
@@ -192,12 +194,21 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
   int32_t chunk = o.kv_chunk;
   if (chunk == 0) {
     int64_t c = (work + target - 1) / std::max(1, target);
-    c = ((c + 63) / 64) * 64;
     chunk = (int32_t)std::min<int64_t>(std::max<int64_t>(c, kMinChunk), 1 << 30);
   }
+  chunk = ((chunk + ps - 1) / ps) * ps;  // chunk boundaries stay page-aligned
+  // a key range of length len is cut into ceil(len / chunk) nearly equal
+  // page-aligned parts (no sliver of a few keys at the end)
+  auto part_of = [&](const Sequence& s) -> int32_t {
+    const int32_t len = s.k_end - s.k_begin;
+    if (len <= 0) return chunk;
+    const int32_t parts = (len + chunk - 1) / chunk;
+    const int32_t even = (len + parts - 1) / parts;
+    return ((even + ps - 1) / ps) * ps;
+  };
   auto n_chunks = [&](const Sequence& s) -> int32_t {
     const int32_t len = s.k_end - s.k_begin;
-    return len <= 0 ? 0 : (len + chunk - 1) / chunk;
+    return len <= 0 ? 0 : (len + part_of(s) - 1) / part_of(s);
   };
 
   // ---- partial slots per output row ------------------------------------
@@ -241,6 +252,7 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
   std::vector<RowDesc> rows;
   for (const Sequence& s : seqs) {
     const int32_t nc = n_chunks(s);
+    const int32_t part = part_of(s);
     for (int32_t h = 0; h < Hkv; ++h) {
       // the rows of this KV head: members x new rows x the g query heads
       struct R { int32_t r, i, hq; };
@@ -251,8 +263,8 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
           for (int32_t j = 0; j < g; ++j) rr.push_back({r, i, h * g + j});
       }
       for (int32_t c = 0; c < nc; ++c) {
-        const int32_t kb = s.k_begin + c * chunk;
-        const int32_t ke = std::min(s.k_end, kb + chunk);
+        const int32_t kb = s.k_begin + c * part;
+        const int32_t ke = std::min(s.k_end, kb + part);
         for (size_t p = 0; p < rr.size(); p += kRowsPerDecodeItem) {
           DecodeItem it = {};
           it.bt_row = s.bt_row;
@@ -277,6 +289,11 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
       }
     }
   }
+
+  // heaviest split-KV CTAs first (the hardware hands out CTAs in order)
+  std::stable_sort(items.begin(), items.end(), [](const DecodeItem& x, const DecodeItem& y) {
+    return (x.k_end - x.k_begin) > (y.k_end - y.k_begin);
+  });
 
   // ---- prefill items, heaviest first -----------------------------------
   std::vector<PrefillItem> pitems;

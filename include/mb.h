@@ -98,8 +98,10 @@ typedef struct {
   int32_t prefill_min_rows;  /* requests with q_rows >= this run the tensor-core
                                 prefill kernel; 0 -> default (16);
                                 < 0 -> never (everything on split-KV)        */
-  int32_t kv_chunk;          /* split-KV chunk in keys (multiple of 64);
-                                0 -> chosen from the batch                   */
+  int32_t kv_chunk;          /* split-KV chunk in keys (multiple of 64, rounded
+                                up to whole pages; ranges are cut into equal
+                                page-aligned parts no longer than this);
+                                0 -> chosen from the batch (>= 1024)         */
   int32_t disable_cascade;   /* 1 -> no shared-prefix grouping               */
   int32_t target_ctas;       /* split-KV work items to aim for; 0 -> auto     */
 } mb_plan_options_t;

@@ -144,7 +144,7 @@ def check_coverage(w, opts=None):
     ps = s.page_size
     covered = {}     # (q_index, q_head) -> list of (k_begin, k_end, slot)
     for it in items:
-        assert 1 <= it["n_rows"] <= 8
+        assert 1 <= it["n_rows"] <= 128
         assert 0 <= it["k_begin"] < it["k_end"]
         for rw in rows[it["row_begin"]:it["row_begin"] + it["n_rows"]]:
             assert rw["q_head"] // g == it["kv_head"]          # one KV head per CTA
