@@ -64,6 +64,11 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true",
                     help="skip the clock-sampling window (profiling runs)")
+    ap.add_argument("--max-requests", type=int, default=0,
+                    help="keep only the first N requests of the workload (small profiling "
+                         "captures of the same kernels)")
+    ap.add_argument("--disable-cascade", action="store_true",
+                    help="plan without shared-prefix grouping (comparison runs)")
     return ap.parse_args(argv)
 
 
@@ -277,6 +282,19 @@ def run_reference(args):
     return 0
 
 
+def truncate(w, n):
+    """The first n requests of a workload (same pages, same values)."""
+    import dataclasses
+    n = min(n, w.n_requests)
+    tq = int(w.requests[n - 1, 1])
+    th = int(w.hist_requests[n - 1, 1])
+    return dataclasses.replace(w, requests=w.requests[:n].copy(),
+                               block_table=w.block_table[:n].copy(), q=w.q[:tq],
+                               k_new=w.k_new[:tq], v_new=w.v_new[:tq],
+                               hist_requests=w.hist_requests[:n].copy(),
+                               k_hist=w.k_hist[:th], v_hist=w.v_hist[:th])
+
+
 def workload_config(w):
     s = w.spec
     return {"workload": s.name, "description": s.description, "q_rows": w.total_q,
@@ -284,6 +302,15 @@ def workload_config(w):
             "head_dim": s.head_dim, "page_size": s.page_size,
             "l2": "flushed between timed steps (256 MiB write, outside the events)",
             "step": "mb_kv_append + mb_attn_plan (host + 1 H2D) + mb_attn_forward"}
+
+
+def workload_config_args(w, args):
+    c = workload_config(w)
+    if args.max_requests:
+        c["max_requests"] = args.max_requests
+    if args.disable_cascade:
+        c["cascade"] = "disabled"
+    return c
 
 
 # --------------------------------------------------------------- GPU arm
@@ -304,7 +331,10 @@ def run_gpu(args):
     B.lib()
 
     w = W.make_workload(args.workload, device=dev)
+    if args.max_requests:
+        w = truncate(w, args.max_requests)
     s = w.spec
+    opts = B.options(disable_cascade=1) if args.disable_cascade else None
     cfg = B.config(s.n_q_heads, s.n_kv_heads, s.head_dim, s.page_size, w.num_pages,
                    w.block_table.shape[1], s.scale or 0.0)
     shape = (w.num_pages, s.n_kv_heads, s.page_size, s.head_dim)
@@ -322,7 +352,7 @@ def run_gpu(args):
     lse = torch.empty((w.total_q, s.n_q_heads), dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    probe = B.Plan(w.requests, w.block_table, cfg, device=dev)
+    probe = B.Plan(w.requests, w.block_table, cfg, device=dev, opts=opts)
     info = probe.info.as_dict()
     ws = probe.workspace
     probe.close()
@@ -330,13 +360,13 @@ def run_gpu(args):
 
     def step(stage_events=None):
         B.kv_append(kc, vc, k_new, v_new, slots, cfg, status)
-        plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=ws)
+        plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=ws, opts=opts)
         plan.forward(q, kc, vc, bt_dev, out, lse, events=stage_events)
         plan.close()
 
     def kernel_pass(stage_events):
         # the same launches with per-stage events (stages back to back)
-        plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=ws)
+        plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=ws, opts=opts)
         plan.forward(q, kc, vc, bt_dev, out, lse, events=stage_events)
         plan.close()
 
@@ -443,7 +473,7 @@ def run_gpu(args):
             dk.copy_(hk, non_blocking=True)
             dv.copy_(hv, non_blocking=True)
             B.kv_append(kc, vc, dk, dv, slots, cfg, status)
-            plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=ws)
+            plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=ws, opts=opts)
             plan.forward(dq, kc, vc, bt_dev, out, lse)
             plan.close()
             hout.copy_(out, non_blocking=True)
@@ -479,7 +509,7 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {**workload_config(w), "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "config": {**workload_config_args(w, args), "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
