@@ -12,8 +12,9 @@
 // Roles (384 threads, three warpgroups):
 //   warps 0-3   softmax of query tile A, warps 4-7 softmax of tile B: one
 //               thread per query row (TMEM lane = row). Load the 128 scores of
-//               the row in one TMEM load, mask, take the running max (log2
-//               domain, scale folded into one FFMA before ex2), write P as
+//               the row in one TMEM load, mask, take the running max (three-
+//               input max), scale and shift two scores per packed f32x2 FMA
+//               before ex2 (log2 domain), sum in packed adds, write P as
 //               bf16 back into TMEM over the row's own scores (the PV MMA
 //               reads its A operand from there), and rescale O in TMEM only
 //               when a row's max grew by more than 2^8. At the end normalise
@@ -30,7 +31,9 @@
 //   warp 9      allocates all 512 TMEM columns (S_A, S_B, O_A, O_B); one lane
 //               issues every MMA: S_X = Q_X K^T (M 128, N 128, K = D, both
 //               operands in shared memory) and O_X += P_X V (M 128, N = D,
-//               K 128, P from TMEM, V from shared memory), ordered
+//               K 128, P from TMEM, V from shared memory), one integer add
+//               per descriptor (the issuing thread's instruction latency, not
+//               the tensor core, sets the pace), ordered
 //                   PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
 //               so that each softmax group has two MMAs' time to turn its
 //               scores into probabilities while the tensor core works for the
@@ -58,8 +61,8 @@ constexpr int kThreads = 384;
 // registers per thread: at launch (ptxas' count under the launch bounds, checked
 // on the host before every launch), then after the re-allocation
 constexpr int kLaunchRegs = 168;
-constexpr int kProducerRegs = 56;
-constexpr int kSoftmaxRegs = 224;
+constexpr int kProducerRegs = 72;
+constexpr int kSoftmaxRegs = 216;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kProducerRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch's register pool");
 constexpr uint32_t kTmemCols = 512;
@@ -250,32 +253,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
-      const uint32_t qa = smem_u32(sq);
-      const uint32_t kva = smem_u32(skv);
+      // Descriptor words (sdesc_sw128): every operand here shares the high
+      // word (SBO 1024); the low words hold the tile's start address and LBO.
+      // Each MMA then costs one integer add per operand: the issuing thread is
+      // latency-bound (it shares its SM sub-partition with two softmax warps),
+      // so every instruction between two MMAs shows up in the step time.
+      const uint32_t d_hi = (uint32_t)(sdesc_sw128(0, 0, 1024) >> 32);
+      const uint32_t q_lo = (uint32_t)sdesc_sw128(smem_u32(sq), 16, 1024);
+      const uint32_t k_lo = (uint32_t)sdesc_sw128(smem_u32(skv), 16, 1024);
+      const uint32_t v_lo = (uint32_t)sdesc_sw128(smem_u32(skv), L::kHalfBytes, 1024);
+      constexpr uint32_t kTileW = L::kTileBytes >> 4;  // one tile in descriptor address units
+      constexpr uint32_t kHalfW = L::kHalfBytes >> 4;
       int committed_o[2] = {-1, -1};
       auto issue_s = [&](int t, int j) {
-        const uint32_t q0 = qa + t * L::kTileBytes;
-        const uint32_t k0 = kva + ((2 * j) % L::kSlots) * L::kTileBytes;
+        const uint32_t a0 = q_lo + t * kTileW;
+        const uint32_t b0 = k_lo + ((2 * j) % L::kSlots) * kTileW;
+        const uint32_t d = tmem + kColS + 128 * t;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // K-major operands: 64-element block kk / 4, 32-byte step inside it
-          const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-          umma_bf16_ss(tmem + kColS + 128 * t, sdesc_sw128(q0 + off, 16, 1024),
-                       sdesc_sw128(k0 + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          const uint32_t o = (kk >> 2) * kHalfW + (kk & 3) * 2;
+          umma_bf16_ss_w(d, a0 + o, b0 + o, d_hi, idesc_qk, (uint32_t)kk);
         }
         umma_commit(&bars[B_S_FULL + t]);
       };
       auto issue_pv = [&](int t, int j) {
-        const uint32_t v0 = kva + ((2 * j + 1) % L::kSlots) * L::kTileBytes;
+        // A = P [128 rows x 128 keys] in TMEM over S_X: 16 keys = 8 columns;
+        // B = V [128 keys x D], MN-major: 16 keys = two 8-row groups (SBO,
+        // 2048 bytes), next 64 head dims one half further (LBO)
+        const uint32_t b0 = v_lo + ((2 * j + 1) % L::kSlots) * kTileW;
+        const uint32_t a0 = tmem + kColS + 128 * t;
+        const uint32_t d = tmem + kColO + 128 * t;
+        const uint32_t acc = j > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // A = P [128 rows x 128 keys] in TMEM over S_X: 16 keys = 8 columns;
-          // B = V [128 keys x D], MN-major: 16 keys = two 8-row groups (SBO),
-          // next 64 head dims one half further (LBO)
-          const uint64_t bd = sdesc_sw128(v0 + kk * 2048, L::kHalfBytes, 1024);
-          umma_bf16_ts(tmem + kColO + 128 * t, tmem + kColS + 128 * t + kk * 8, bd, idesc_pv,
-                       (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_bf16_ts_w(d, a0 + kk * 8, b0 + kk * 128, d_hi, idesc_pv, acc | (uint32_t)kk);
         umma_commit(&bars[B_O_DONE + t]);
         committed_o[t] = j;
       };
@@ -349,18 +361,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 128; ++e)
           if (e > lim) s[e] = __float_as_uint(-INFINITY);
       }
-      float mx[16];
+      // row max: three-input max over 128 scores, 8 independent chains
+      float mx[8];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) mx[k] = __uint_as_float(s[k]);
+      for (int k = 0; k < 8; ++k)
+        mx[k] = fmax3(__uint_as_float(s[k]), __uint_as_float(s[k + 8]), __uint_as_float(s[k + 16]));
 #pragma unroll
-      for (int e = 16; e < 128; e += 16)
+      for (int e = 24; e < 120; e += 16)
 #pragma unroll
-        for (int k = 0; k < 16; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(s[e + k]));
+        for (int k = 0; k < 8; ++k)
+          mx[k] = fmax3(mx[k], __uint_as_float(s[e + k]), __uint_as_float(s[e + 8 + k]));
 #pragma unroll
-      for (int w2 = 8; w2 > 0; w2 >>= 1)
-#pragma unroll
-        for (int k = 0; k < w2; ++k) mx[k] = fmaxf(mx[k], mx[k + w2]);
-      const float tmax = mx[0];
+      for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(s[120 + k]));
+      const float tmax =
+          fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       const float m_new = fmaxf(m, tmax);
       // lazy rescale: keep the old max unless it grew by more than 2^8
       float alpha = 1.f;
@@ -376,15 +390,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float mc = (m == -INFINITY) ? 0.f : m * c;
-      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+      // p = 2^(s * c - m * c): the scale-and-shift of two scores in one
+      // packed FMA, the row sum in two packed accumulators
+      const uint64_t c2 = f32x2(c, c), nmc2 = f32x2(-mc, -mc);
+      uint64_t acc[2] = {0ull, 0ull};
       uint32_t pk[64];
 #pragma unroll
       for (int e = 0; e < 128; e += 2) {
-        const float e0 = fast_exp2(fmaf(__uint_as_float(s[e]), c, -mc));
-        const float e1 = fast_exp2(fmaf(__uint_as_float(s[e + 1]), c, -mc));
-        sum[(e >> 1) & 3] += e0 + e1;
+        float x0, x1;
+        f32x2_split(ffma_x2(f32x2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), c2, nmc2),
+                    x0, x1);
+        const float e0 = fast_exp2(x0);
+        const float e1 = fast_exp2(x1);
+        acc[(e >> 1) & 1] = fadd_x2(acc[(e >> 1) & 1], f32x2(e0, e1));
         pk[e >> 1] = pack_bf16x2(e0, e1);
       }
+      float sum_lo, sum_hi;
+      f32x2_split(fadd_x2(acc[0], acc[1]), sum_lo, sum_hi);
       // O_t may be touched once its previous PV has completed
       if (j > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + t], (uint32_t)(j - 1) & 1u,
@@ -407,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       tmem_st32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       tmem_st_wait();
-      l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+      l += sum_lo + sum_hi;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_P_FULL + t]);

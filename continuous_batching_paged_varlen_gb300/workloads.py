@@ -14,7 +14,9 @@ the Llama-2-7B single-layer ORCA iteration of "ORCA and chunked prefill", §2
 batch; a chunked-prefill chunk (2048 rows at S0 = 30720) beside decodes, as in
 "ORCA and chunked prefill", §4-§5; and the shared-prefix decode step of "How
 To Scale Your Model notes (7-8)", §3 (six requests sharing 4096 positions plus
-1024 private each). Values are fp32 N(0, 1) rounded to bf16.
+1024 private each). Two more shapes (``EXTRA``): speculative decode steps of
+k + 1 rows, and a prefill-only ragged batch. Values are fp32 N(0, 1) rounded
+to bf16.
 """
 
 from __future__ import annotations
@@ -36,7 +38,8 @@ class WorkloadSpec:
     page_size: int
     # fixed (q_rows, kv_length) per request, or None when drawn from ``draw``
     requests: Optional[tuple] = None
-    # random part: list of (count, q_rows, kv_lo, kv_hi) drawn uniformly
+    # random part: list of (count, q_rows, kv_lo, kv_hi) drawn uniformly;
+    # q_rows None means q_rows = kv_length (a whole prompt, S0 = 0)
     draw: Optional[tuple] = None
     # positions shared (same physical pages) by every request; must be a
     # multiple of page_size
@@ -79,11 +82,28 @@ SPECS = {
         description="6 decodes q 1, kv 5121, sharing the physical pages of a "
                     "4096-position prefix + 1025 private positions each; "
                     "Hq 32 / Hkv 8, D 128, page 64"),
+    # two further shapes the same triple expresses
+    "spec_decode_k3": WorkloadSpec(
+        name="spec_decode_k3", n_q_heads=32, n_kv_heads=8, head_dim=128,
+        page_size=64, draw=((64, 4, 1024, 8192),), seed=6,
+        description="64 speculative-decode steps of k + 1 = 4 rows each (3 draft "
+                    "tokens + 1), kv ~ U{1024..8192}; Hq 32 / Hkv 8, D 128, page 64"),
+    "varlen_prefill": WorkloadSpec(
+        name="varlen_prefill", n_q_heads=32, n_kv_heads=8, head_dim=128,
+        page_size=64, draw=((16, None, 128, 4096),), seed=7,
+        description="prefill-only varlen batch (cu_seqlens style): 16 requests, "
+                    "q_rows = kv ~ U{128..4096}, S0 = 0; Hq 32 / Hkv 8, D 128, page 64"),
 }
 
 # The order the pages' workloads are usually listed in.
 ORDER = ["tiny_mixed", "llama2_7b_orca_iteration", "decode_heavy_gqa4",
          "chunked_prefill_mix", "shared_prefix_decode"]
+# Further shapes: several new rows per decode step (speculative / MTP
+# verification, "GLM-5.3 e2e token ledger", stage 3: up to k + 1 tokens per
+# running request) and a prefill-only ragged batch ("One forward, many
+# requests", §6: cu_seqlens over a flat token buffer).
+EXTRA = ["spec_decode_k3", "varlen_prefill"]
+ALL = ORDER + EXTRA
 
 
 @dataclasses.dataclass
@@ -125,7 +145,7 @@ def request_shapes(spec: WorkloadSpec) -> list:
         rng = np.random.default_rng(spec.seed)
         for count, q_rows, lo, hi in spec.draw:
             kvs = rng.integers(lo, hi + 1, size=count)
-            shapes += [(q_rows, int(kv)) for kv in kvs]
+            shapes += [(int(kv) if q_rows is None else q_rows, int(kv)) for kv in kvs]
     return shapes
 
 

@@ -132,6 +132,32 @@ def test_chunked_prefill_mix_parity_sampled():
         assert_request_close(w, out, lse, r)
 
 
+def test_spec_decode_parity_sampled():
+    # k + 1 = 4 new rows per request: causal among the step's own rows
+    w = W.make_workload("spec_decode_k3", device="cuda")
+    kc, vc, cfg = fill_cache(w)
+    out, lse, status, info = run_forward(w, kc, vc, cfg)
+    assert status == 0 and info["n_prefill_items"] == 0
+    assert torch.isfinite(out.float()).all()
+    rng = np.random.default_rng(1)
+    for r in sorted(rng.choice(w.n_requests, 8, replace=False).tolist()) + [0, w.n_requests - 1]:
+        assert_request_close(w, out, lse, r)
+
+
+def test_varlen_prefill_parity_sampled():
+    # prefill-only ragged batch (S0 = 0 everywhere): each request's own causal
+    # block only, never a cross-request block
+    w = W.make_workload("varlen_prefill", device="cuda")
+    kc, vc, cfg = fill_cache(w)
+    out, lse, status, info = run_forward(w, kc, vc, cfg)
+    assert status == 0 and info["n_decode_items"] == 0
+    assert torch.isfinite(out.float()).all()
+    for r in [0, 5, 11, w.n_requests - 1]:
+        m = int(w.requests[r, 1] - w.requests[r, 0])
+        for a, b in [(0, 40), (m // 2 - 20, m // 2 + 20), (m - 40, m)]:
+            assert_request_close(w, out, lse, r, heads=[0, 17, 31], rows=(a, b))
+
+
 @pytest.mark.parametrize("cascade", [True, False])
 def test_shared_prefix_parity(cascade):
     w = W.make_workload("shared_prefix_decode", device="cuda")
