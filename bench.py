@@ -398,10 +398,13 @@ def run_gpu(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
+    host_s = 0.0
     for i in range(K):
         flush.zero_()
         ev[i][0].record(stream)
+        h0 = time.perf_counter()
         step()
+        host_s += time.perf_counter() - h0
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -519,6 +522,10 @@ def run_gpu(args):
                      "algorithmic_flops_per_step": work["total_flops"],
                      "algorithmic_bytes_per_step": work["total_bytes"] + work["append_bytes"]},
         "plan": info, "device_status": dev_status, "wall_s_timed_region": wall,
+        # host time to enqueue one step (append, plan + upload, forward, through
+        # the Python binding); a step shorter than this on the device is
+        # host-bound, the GPU waiting for its launches
+        "host_enqueue_us_per_step": host_s / K * 1e6,
     }
     if rank == 0:
         print(json.dumps(line))

@@ -169,10 +169,11 @@ mb_status_t mb_attn_forward_timed(const mb_plan_t* plan, const void* q, const vo
   }
   if (d.n_combine > 0) {
     rec(MB_STAGE_COMBINE, 0);
+    // overlaps the split-KV kernel's tail (every combine row comes from it)
     e = launch_combine(reinterpret_cast<const CombineEntry*>(ws + d.off_combine), d.n_combine,
                        reinterpret_cast<const float*>(ws + d.off_part_o),
                        reinterpret_cast<const float*>(ws + d.off_part_lse), d.head_dim,
-                       d.n_q_heads, out, lse, stream);
+                       d.n_q_heads, out, lse, stream, events == nullptr);
     rec(MB_STAGE_COMBINE, 1);
     if (e != cudaSuccess) return MB_ERR_CUDA;
   }

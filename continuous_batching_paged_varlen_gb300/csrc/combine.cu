@@ -10,7 +10,7 @@
 // Partials carry base-2 LSEs; the final LSE is written in natural log.
 //
 // One warp per output row; lanes over head dims, so every partial row is
-// read with coalesced loads.
+// read with coalesced loads, and the slots' weights computed one per lane.
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -30,6 +30,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineEntry* __rest
                                                       int32_t Hq, __nv_bfloat16* __restrict__ out,
                                                       float* __restrict__ lse) {
   constexpr int DL = D / 32;
+  // launched to overlap the split-KV kernel's tail: wait here until that grid
+  // has finished and its partials are visible (returns at once otherwise)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (w >= n) return;
@@ -42,13 +45,35 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineEntry* __rest
 #pragma unroll
   for (int k = 0; k < DL; ++k) O[k] = 0.f;
   if (M != -INFINITY) {
-    for (int s = 0; s < e.n_slots; ++s) {
-      const int64_t slot = e.slot_begin + s;
-      const float f = dev::fast_exp2(part_lse[slot] - M);
-      L += f;
+    for (int s0 = 0; s0 < e.n_slots; s0 += 32) {
+      // the weights of up to 32 slots, one per lane; the rows of four slots
+      // are loaded before any is accumulated (the loop is latency-bound)
+      const int ns = min(32, e.n_slots - s0);
+      const float wl = lane < ns ? dev::fast_exp2(part_lse[e.slot_begin + s0 + lane] - M) : 0.f;
+      L += wl;
+      const float* base = part_o + (int64_t)(e.slot_begin + s0) * D + lane;
+      int s = 0;
+      for (; s + 4 <= ns; s += 4) {
+        float v[4][DL];
 #pragma unroll
-      for (int k = 0; k < DL; ++k) O[k] = fmaf(f, part_o[slot * D + lane + 32 * k], O[k]);
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int k = 0; k < DL; ++k) v[u][k] = base[(int64_t)(s + u) * D + 32 * k];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float f = __shfl_sync(0xffffffffu, wl, s + u);
+#pragma unroll
+          for (int k = 0; k < DL; ++k) O[k] = fmaf(f, v[u][k], O[k]);
+        }
+      }
+      for (; s < ns; ++s) {
+        const float f = __shfl_sync(0xffffffffu, wl, s);
+#pragma unroll
+        for (int k = 0; k < DL; ++k) O[k] = fmaf(f, base[(int64_t)s * D + 32 * k], O[k]);
+      }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   }
   const int64_t orow = (int64_t)e.q_index * Hq + e.q_head;
   const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -61,17 +86,24 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineEntry* __rest
 
 cudaError_t launch_combine(const CombineEntry* entries, int32_t n, const float* part_o,
                            const float* part_lse, int32_t head_dim, int32_t n_q_heads,
-                           void* out, float* lse, cudaStream_t s) {
+                           void* out, float* lse, cudaStream_t s, bool overlap_previous) {
   if (n <= 0) return cudaSuccess;
   const int warps = 8;
-  const unsigned blocks = (unsigned)((n + warps - 1) / warps);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((n + warps - 1) / warps));
+  cfg.blockDim = dim3(warps * 32);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_previous ? 1 : 0;
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
   if (head_dim == 128)
-    combine_kernel<128><<<blocks, warps * 32, 0, s>>>(entries, n, part_o, part_lse, n_q_heads,
-                                                       (__nv_bfloat16*)out, lse);
-  else
-    combine_kernel<64><<<blocks, warps * 32, 0, s>>>(entries, n, part_o, part_lse, n_q_heads,
-                                                      (__nv_bfloat16*)out, lse);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, combine_kernel<128>, entries, n, part_o, part_lse,
+                              n_q_heads, o, lse);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<64>, entries, n, part_o, part_lse, n_q_heads,
+                            o, lse);
 }
 
 }  // namespace mb

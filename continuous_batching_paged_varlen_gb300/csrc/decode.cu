@@ -97,6 +97,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
 
+  // the combine kernel launched after this one (programmatic stream
+  // serialization) may be scheduled now; it waits for this grid to finish
+  // before it reads the partials
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   const DecodeItem it = a.items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nr = it.n_rows;

@@ -39,10 +39,13 @@ struct DecodeArgs {
 // produce anything it reads) is still running.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, bool overlap_previous = false);
 
-// LSE merge of partials (combine.cu).
+// LSE merge of partials (combine.cu). overlap_previous: launch with
+// programmatic stream serialization after the split-KV kernel (the combine
+// kernel waits for that grid's completion before reading partials).
 cudaError_t launch_combine(const CombineEntry* entries, int32_t n, const float* part_o,
                            const float* part_lse, int32_t head_dim, int32_t n_q_heads,
-                           void* out, float* lse, cudaStream_t s);
+                           void* out, float* lse, cudaStream_t s,
+                           bool overlap_previous = false);
 
 // tcgen05 prefill kernel (prefill.cu).
 struct PrefillArgs {

@@ -10,7 +10,6 @@
 #include <string.h>
 
 #include <algorithm>
-#include <map>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -24,10 +23,20 @@ using namespace mb;
 namespace {
 
 constexpr int kDefaultPrefillMinRows = 16;
-// split-KV CTAs to aim for (one resident CTA per SM, ~2 waves on 152 SMs)
-constexpr int kDefaultTargetCtas = 2 * 152;
-// shortest automatic split-KV chunk: 8 key tiles amortise a CTA's set-up
+// SMs of the GPU the planner sizes work for (a GB300); the split-KV kernel
+// keeps one CTA per SM
+constexpr int kSms = 152;
+// split-KV CTAs to aim for on large batches (~2 waves)
+constexpr int kDefaultTargetCtas = 2 * kSms;
+// shortest automatic split-KV chunk on large batches: 8 key tiles amortise a
+// CTA's set-up
 constexpr int kMinChunk = 1024;
+// A batch with at most this many 128-key tiles of split-KV work (summed over
+// CTAs as if unsplit) is latency-bound: its chunks are sized so that the CTAs
+// fill one wave of SMs with as few tiles each as possible (but at least
+// kMinSmallChunk keys, so set-up stays a minority of a CTA's time).
+constexpr int64_t kSmallBatchTiles = (int64_t)kSms * 8;
+constexpr int kMinSmallChunk = 256;
 
 bool is_pow2_in(int v, int lo, int hi) {
   return v >= lo && v <= hi && (v & (v - 1)) == 0;
@@ -89,9 +98,33 @@ namespace {
 struct Sequence {       // one key range walked by split-KV CTAs
   int32_t bt_row;
   int32_t k_begin, k_end;
-  std::vector<int32_t> members;  // requests whose rows attend to it
+  int32_t mbeg, mend;   // requests whose rows attend to it: member_list[mbeg, mend)
   bool shared;
 };
+
+// Indices 0..n-1 ordered by key (>= 0) descending, ties in index order (the
+// plan's heaviest-first CTA order): a stable counting sort over the key range
+// when it is small (keys are tile or key counts), else one sort of packed
+// 64-bit keys; the work items themselves are moved once, by the caller.
+template <typename KeyFn>
+std::vector<int32_t> heavy_first(size_t n, KeyFn key) {
+  std::vector<int32_t> order(n);
+  int32_t kmax = 0;
+  for (size_t i = 0; i < n; ++i) kmax = std::max(kmax, key(i));
+  if (kmax <= (int32_t)std::max<size_t>(4 * n, 1 << 16)) {
+    std::vector<int32_t> start((size_t)kmax + 2, 0);
+    for (size_t i = 0; i < n; ++i) ++start[(size_t)(kmax - key(i)) + 1];
+    for (size_t b = 1; b < start.size(); ++b) start[b] += start[b - 1];
+    for (size_t i = 0; i < n; ++i) order[start[(size_t)(kmax - key(i))]++] = (int32_t)i;
+    return order;
+  }
+  std::vector<uint64_t> k(n);
+  for (size_t i = 0; i < n; ++i)
+    k[i] = ((uint64_t)(uint32_t)(INT32_MAX - key(i)) << 32) | (uint32_t)i;
+  std::sort(k.begin(), k.end());
+  for (size_t i = 0; i < n; ++i) order[i] = (int32_t)(k[i] & 0xffffffffu);
+  return order;
+}
 
 }  // namespace
 
@@ -127,72 +160,100 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
   }
 
   // ---- shared-prefix groups among split-KV requests -------------------
+  // requests are grouped by the physical page of their first block (a sort
+  // of (page, request) pairs); a group of two or more then shares the
+  // longest run of leading blocks that every member maps to the same pages
   std::vector<int32_t> own_begin(n, 0);
   std::vector<Sequence> seqs;
+  std::vector<int32_t> member_list;
+  seqs.reserve(decode_reqs.size() + 1);
+  member_list.reserve(2 * decode_reqs.size());
   int32_t n_groups = 0, cascade_keys = 0;
   if (!o.disable_cascade) {
-    std::map<int32_t, std::vector<int32_t>> by_first;
+    std::vector<uint64_t> firsts;
+    firsts.reserve(decode_reqs.size());
     for (int32_t r : decode_reqs) {
       const int32_t s0 = reqs[r].kv_length - (reqs[r].q_end - reqs[r].q_start);
-      if (s0 >= ps) by_first[bt[(size_t)r * mb]].push_back(r);
+      if (s0 >= ps) firsts.push_back(((uint64_t)(uint32_t)bt[(size_t)r * mb] << 32) | (uint32_t)r);
     }
-    for (auto& kv : by_first) {
-      std::vector<int32_t>& mem = kv.second;
-      if (mem.size() < 2) continue;
-      // longest run of leading blocks that every member maps to the same
-      // physical page and that lies wholly inside every member's cache
-      int32_t L = 0;
-      for (;; ++L) {
-        bool ok = true;
-        // (L + 1) * ps <= s0 <= kv_length keeps L inside every member's
-        // validated block-table entries; check it before reading entry L
-        for (int32_t r : mem) {
-          const int32_t s0 = reqs[r].kv_length - (reqs[r].q_end - reqs[r].q_start);
-          if ((int64_t)(L + 1) * ps > s0) ok = false;
-        }
-        if (!ok) break;
-        const int32_t page = bt[(size_t)mem[0] * mb + L];
-        for (int32_t r : mem) {
-          if (bt[(size_t)r * mb + L] != page) {
-            ok = false;
-            break;
+    std::sort(firsts.begin(), firsts.end());
+    for (size_t a = 0; a < firsts.size();) {
+      size_t b = a + 1;
+      while (b < firsts.size() && (firsts[b] >> 32) == (firsts[a] >> 32)) ++b;
+      if (b - a >= 2) {
+        const int32_t mbeg = (int32_t)member_list.size();
+        for (size_t x = a; x < b; ++x) member_list.push_back((int32_t)(firsts[x] & 0xffffffffu));
+        const int32_t mend = (int32_t)member_list.size();
+        // longest run of leading blocks that every member maps to the same
+        // physical page and that lies wholly inside every member's cache
+        int32_t L = 0;
+        for (;; ++L) {
+          bool ok = true;
+          // (L + 1) * ps <= s0 <= kv_length keeps L inside every member's
+          // validated block-table entries; check it before reading entry L
+          for (int32_t x = mbeg; x < mend && ok; ++x) {
+            const int32_t r = member_list[x];
+            const int32_t s0 = reqs[r].kv_length - (reqs[r].q_end - reqs[r].q_start);
+            if ((int64_t)(L + 1) * ps > s0) ok = false;
           }
+          if (!ok) break;
+          const int32_t page = bt[(size_t)member_list[mbeg] * mb + L];
+          for (int32_t x = mbeg; x < mend && ok; ++x)
+            if (bt[(size_t)member_list[x] * mb + L] != page) ok = false;
+          if (!ok) break;
         }
-        if (!ok) break;
+        if (L >= 1) {
+          Sequence sq;
+          sq.bt_row = member_list[mbeg];
+          sq.k_begin = 0;
+          sq.k_end = L * ps;
+          sq.mbeg = mbeg;
+          sq.mend = mend;
+          sq.shared = true;
+          seqs.push_back(sq);
+          for (int32_t x = mbeg; x < mend; ++x) own_begin[member_list[x]] = L * ps;
+          ++n_groups;
+          cascade_keys += L * ps;
+        } else {
+          member_list.resize(mbeg);
+        }
       }
-      if (L < 1) continue;
-      Sequence s;
-      s.bt_row = mem[0];
-      s.k_begin = 0;
-      s.k_end = L * ps;
-      s.members = mem;
-      s.shared = true;
-      seqs.push_back(s);
-      for (int32_t r : mem) own_begin[r] = L * ps;
-      ++n_groups;
-      cascade_keys += L * ps;
+      a = b;
     }
   }
   for (int32_t r : decode_reqs) {
-    Sequence s;
-    s.bt_row = r;
-    s.k_begin = own_begin[r];
-    s.k_end = reqs[r].kv_length;
-    s.members = {r};
-    s.shared = false;
-    seqs.push_back(s);
+    Sequence sq;
+    sq.bt_row = r;
+    sq.k_begin = own_begin[r];
+    sq.k_end = reqs[r].kv_length;
+    sq.mbeg = (int32_t)member_list.size();
+    member_list.push_back(r);
+    sq.mend = sq.mbeg + 1;
+    sq.shared = false;
+    seqs.push_back(sq);
   }
 
   // ---- split-KV chunk size ---------------------------------------------
-  int64_t work = 0;  // key-visits summed over CTAs if nothing were split
+  int64_t work = 0;   // key-visits summed over CTAs if nothing were split
+  int64_t tiles = 0;  // the same in 128-key tiles
   for (const Sequence& s : seqs) {
     int64_t rows = 0;
-    for (int32_t r : s.members) rows += (int64_t)(reqs[r].q_end - reqs[r].q_start) * g;
+    for (int32_t x = s.mbeg; x < s.mend; ++x) {
+      const int32_t r = member_list[x];
+      rows += (int64_t)(reqs[r].q_end - reqs[r].q_start) * g;
+    }
     const int64_t groups = (rows + kRowsPerDecodeItem - 1) / kRowsPerDecodeItem;
     work += (int64_t)(s.k_end - s.k_begin) * groups * Hkv;
+    tiles += (int64_t)((s.k_end - s.k_begin + 127) / 128) * groups * Hkv;
   }
   int32_t chunk = o.kv_chunk;
-  if (chunk == 0) {
+  const bool one_wave = chunk == 0 && o.target_ctas == 0 && tiles <= kSmallBatchTiles;
+  if (one_wave) {
+    // start from ceil(tiles / SMs) tiles per CTA; the search below grows it
+    // until page rounding leaves no CTA for a second wave
+    const int64_t per = (tiles + kSms - 1) / kSms;
+    chunk = (int32_t)std::max<int64_t>(per * 128, kMinSmallChunk);
+  } else if (chunk == 0) {
     int64_t c = (work + target - 1) / std::max(1, target);
     chunk = (int32_t)std::min<int64_t>(std::max<int64_t>(c, kMinChunk), 1 << 30);
   }
@@ -206,6 +267,25 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
     const int32_t even = (len + parts - 1) / parts;
     return ((even + ps - 1) / ps) * ps;
   };
+  if (one_wave) {
+    auto ctas = [&]() -> int64_t {
+      int64_t c = 0;
+      for (const Sequence& s : seqs) {
+        const int32_t len = s.k_end - s.k_begin;
+        if (len <= 0) continue;
+        int64_t rows = 0;
+        for (int32_t x = s.mbeg; x < s.mend; ++x) {
+          const int32_t r = member_list[x];
+          rows += (int64_t)(reqs[r].q_end - reqs[r].q_start) * g;
+        }
+        const int64_t groups = (rows + kRowsPerDecodeItem - 1) / kRowsPerDecodeItem;
+        c += (int64_t)((len + part_of(s) - 1) / part_of(s)) * groups * Hkv;
+      }
+      return c;
+    };
+    const int step = std::max(ps, 128);
+    for (int guard = 0; guard < 4096 && ctas() > kSms; ++guard) chunk += step;
+  }
   auto n_chunks = [&](const Sequence& s) -> int32_t {
     const int32_t len = s.k_end - s.k_begin;
     return len <= 0 ? 0 : (len + part_of(s) - 1) / part_of(s);
@@ -216,7 +296,8 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
   // slots: first the chunks of its shared prefix (if any), then its own.
   std::vector<int32_t> shared_chunks(n, 0), own_chunks(n, 0), slot_base(n, -1);
   for (const Sequence& s : seqs)
-    for (int32_t r : s.members) {
+    for (int32_t x = s.mbeg; x < s.mend; ++x) {
+      const int32_t r = member_list[x];
       if (s.shared)
         shared_chunks[r] = n_chunks(s);
       else
@@ -248,55 +329,78 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
   };
 
   // ---- split-KV items and row descriptors -----------------------------
+  // per (sequence, KV head, key chunk): the rows of every member request x
+  // its new rows x the g query heads of the KV head, 128 rows per CTA
+  size_t est_items = 0, est_rows = 0;
+  for (const Sequence& s : seqs) {
+    int64_t rs = 0;
+    for (int32_t x = s.mbeg; x < s.mend; ++x) {
+      const int32_t r = member_list[x];
+      rs += (int64_t)(reqs[r].q_end - reqs[r].q_start) * g;
+    }
+    const int64_t nc = n_chunks(s);
+    est_items += (size_t)(nc * Hkv * ((rs + kRowsPerDecodeItem - 1) / kRowsPerDecodeItem));
+    est_rows += (size_t)(nc * Hkv * rs);
+  }
   std::vector<DecodeItem> items;
   std::vector<RowDesc> rows;
+  items.reserve(est_items);
+  rows.reserve(est_rows);
   for (const Sequence& s : seqs) {
     const int32_t nc = n_chunks(s);
     const int32_t part = part_of(s);
     for (int32_t h = 0; h < Hkv; ++h) {
-      // the rows of this KV head: members x new rows x the g query heads
-      struct R { int32_t r, i, hq; };
-      std::vector<R> rr;
-      for (int32_t r : s.members) {
-        const int32_t m = reqs[r].q_end - reqs[r].q_start;
-        for (int32_t i = 0; i < m; ++i)
-          for (int32_t j = 0; j < g; ++j) rr.push_back({r, i, h * g + j});
-      }
       for (int32_t c = 0; c < nc; ++c) {
         const int32_t kb = s.k_begin + c * part;
         const int32_t ke = std::min(s.k_end, kb + part);
-        for (size_t p = 0; p < rr.size(); p += kRowsPerDecodeItem) {
-          DecodeItem it = {};
-          it.bt_row = s.bt_row;
-          it.kv_head = h;
-          it.k_begin = kb;
-          it.k_end = ke;
-          it.row_begin = (int32_t)rows.size();
-          it.n_rows = (int32_t)std::min<size_t>(kRowsPerDecodeItem, rr.size() - p);
-          for (int32_t k = 0; k < it.n_rows; ++k) {
-            const R& x = rr[p + k];
-            const mb_request_t& q = reqs[x.r];
-            const int32_t s0 = q.kv_length - (q.q_end - q.q_start);
-            RowDesc d;
-            d.q_index = q.q_start + x.i;
-            d.q_head = x.hq;
-            d.vis_end = s0 + x.i + 1;
-            d.dst = slot_of(x.r, x.i, x.hq, s.shared, c);
-            rows.push_back(d);
-          }
-          items.push_back(it);
+        DecodeItem it = {};
+        it.bt_row = s.bt_row;
+        it.kv_head = h;
+        it.k_begin = kb;
+        it.k_end = ke;
+        it.row_begin = (int32_t)rows.size();
+        for (int32_t x = s.mbeg; x < s.mend; ++x) {
+          const int32_t r = member_list[x];
+          const mb_request_t& q = reqs[r];
+          const int32_t m = q.q_end - q.q_start, s0 = q.kv_length - m;
+          for (int32_t i = 0; i < m; ++i)
+            for (int32_t jg = 0; jg < g; ++jg) {
+              if ((int32_t)rows.size() - it.row_begin == kRowsPerDecodeItem) {
+                it.n_rows = kRowsPerDecodeItem;
+                items.push_back(it);
+                it.row_begin = (int32_t)rows.size();
+              }
+              RowDesc d;
+              d.q_index = q.q_start + i;
+              d.q_head = h * g + jg;
+              d.vis_end = s0 + i + 1;
+              d.dst = slot_of(r, i, d.q_head, s.shared, c);
+              rows.push_back(d);
+            }
         }
+        it.n_rows = (int32_t)rows.size() - it.row_begin;
+        if (it.n_rows > 0) items.push_back(it);
       }
     }
   }
 
   // heaviest split-KV CTAs first (the hardware hands out CTAs in order)
-  std::stable_sort(items.begin(), items.end(), [](const DecodeItem& x, const DecodeItem& y) {
-    return (x.k_end - x.k_begin) > (y.k_end - y.k_begin);
-  });
+  {
+    const std::vector<int32_t> order =
+        heavy_first(items.size(), [&](size_t i) { return items[i].k_end - items[i].k_begin; });
+    std::vector<DecodeItem> sorted(items.size());
+    for (size_t i = 0; i < order.size(); ++i) sorted[i] = items[order[i]];
+    items.swap(sorted);
+  }
 
   // ---- prefill items, heaviest first -----------------------------------
   std::vector<PrefillItem> pitems;
+  {
+    size_t np = 0;
+    for (int32_t r : prefill_reqs)
+      np += (size_t)Hq * ((reqs[r].q_end - reqs[r].q_start + kPrefillCtaRows - 1) / kPrefillCtaRows);
+    pitems.reserve(np);
+  }
   for (int32_t r : prefill_reqs) {
     const mb_request_t& q = reqs[r];
     const int32_t m = q.q_end - q.q_start, s0 = q.kv_length - m;
@@ -315,10 +419,13 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
         pitems.push_back(p);
       }
   }
-  std::stable_sort(pitems.begin(), pitems.end(),
-                   [](const PrefillItem& a, const PrefillItem& b) {
-                     return a.n_kv_tiles > b.n_kv_tiles;
-                   });
+  {
+    const std::vector<int32_t> order =
+        heavy_first(pitems.size(), [&](size_t i) { return pitems[i].n_kv_tiles; });
+    std::vector<PrefillItem> sorted(pitems.size());
+    for (size_t i = 0; i < order.size(); ++i) sorted[i] = pitems[order[i]];
+    pitems.swap(sorted);
+  }
 
   // ---- workspace layout + host image -----------------------------------
   PlanDevice& d = plan->dev;
