@@ -15,10 +15,13 @@ attention
 brute
     The same attention written as pure-Python loops with ``math.exp`` for
     tiny inputs; it cross-checks ``attention``.
+rope
+    The rotary embedding fused into the KV append (rotate-half pairs at the
+    token's position, the fp64 angle table) and the fused append itself.
 
 Every function is pinned by ``tests/test_oracle.py`` (worked example,
 special cases reducing to library routines, closed forms, invariants and
 brute force). No function is unpinned.
 """
 
-from . import attention, brute  # noqa: F401
+from . import attention, brute, rope  # noqa: F401
