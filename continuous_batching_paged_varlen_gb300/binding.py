@@ -84,6 +84,13 @@ def lib():
     L.mb_slot_mapping.argtypes = [_vp, _i32, _vp, ctypes.POINTER(Config), _vp, _i32]
     L.mb_kv_append.restype = ctypes.c_int
     L.mb_kv_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, ctypes.POINTER(Config), _vp, _vp]
+    L.mb_positions.restype = ctypes.c_int
+    L.mb_positions.argtypes = [_vp, _i32, _vp, _i32]
+    L.mb_rope_table.restype = ctypes.c_int
+    L.mb_rope_table.argtypes = [_vp, _i32, _i32, ctypes.c_float]
+    L.mb_rope_kv_append.restype = ctypes.c_int
+    L.mb_rope_kv_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32,
+                                    ctypes.POINTER(Config), _vp, _vp]
     L.mb_attn_plan.restype = ctypes.c_int
     L.mb_attn_plan.argtypes = [_vp, _i32, _vp, ctypes.POINTER(Config), _vp,
                                ctypes.POINTER(ctypes.c_size_t), _vp, ctypes.POINTER(_vp)]
@@ -159,6 +166,37 @@ def kv_append(k_cache, v_cache, k_new, v_new, slots, cfg: Config, status=None, s
                              _ptr(slots), T, ctypes.byref(cfg), _ptr(status),
                              _stream_ptr(stream) if T else None),
           "mb_kv_append")
+
+
+def positions(requests, total_q: int) -> np.ndarray:
+    """``mb_positions``: logical position of every new row (host int32)."""
+    reqs = _host_i32(requests).reshape(-1, 3)
+    out = np.empty(max(total_q, 1), dtype=np.int32)
+    check(lib().mb_positions(reqs.ctypes.data, reqs.shape[0], out.ctypes.data, total_q),
+          "mb_positions")
+    return out[:total_q]
+
+
+def rope_table(max_position: int, head_dim: int, base: float = 10000.0) -> np.ndarray:
+    """``mb_rope_table``: host fp32 [max_position, head_dim] angle table."""
+    out = np.empty((max_position, head_dim), dtype=np.float32)
+    check(lib().mb_rope_table(out.ctypes.data, max_position, head_dim, float(base)),
+          "mb_rope_table")
+    return out
+
+
+def rope_kv_append(q, k_cache, v_cache, k_new, v_new, positions_dev, slots, cos_sin,
+                   cfg: Config, status=None, stream=None):
+    """``mb_rope_kv_append`` on torch tensors: rotates ``q`` in place, writes the
+    rotated ``k_new`` and ``v_new`` into the caches (``positions_dev``,
+    ``slots``: int32 device tensors; ``cos_sin``: fp32 device table)."""
+    T = int(slots.numel())
+    check(lib().mb_rope_kv_append(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new),
+                                  _ptr(v_new), _ptr(positions_dev), _ptr(slots), T,
+                                  _ptr(cos_sin), int(cos_sin.shape[0]) if cos_sin is not None else 0,
+                                  ctypes.byref(cfg), _ptr(status),
+                                  _stream_ptr(stream) if T else None),
+          "mb_rope_kv_append")
 
 
 class HostPlan:

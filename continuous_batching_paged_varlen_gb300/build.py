@@ -18,8 +18,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmb.so")
-SOURCES = ["plan.cpp", "api.cu", "kv_append.cu", "decode.cu", "combine.cu", "prefill.cu",
-           "noalloc.cu"]
+SOURCES = ["plan.cpp", "api.cu", "kv_append.cu", "rope_append.cu", "decode.cu", "combine.cu",
+           "prefill.cu", "noalloc.cu"]
 HEADERS = ["mb_internal.h", "mb_device.cuh", "kernels.h", "plan_impl.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

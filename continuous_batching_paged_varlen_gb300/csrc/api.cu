@@ -71,6 +71,47 @@ mb_status_t mb_kv_append(void* k_cache, void* v_cache, const void* k_new, const 
   return e == cudaSuccess ? MB_OK : MB_ERR_CUDA;
 }
 
+mb_status_t mb_rope_table(float* cos_sin, int32_t max_position, int32_t head_dim, float base) {
+  if (!cos_sin || max_position <= 0 || head_dim <= 0 || (head_dim & 1) || !(base > 0.0f) ||
+      !isfinite(base))
+    return MB_ERR_INVALID_ARG;
+  const int half = head_dim / 2;
+  for (int32_t p = 0; p < max_position; ++p) {
+    float* row = cos_sin + (size_t)p * head_dim;
+    for (int i = 0; i < half; ++i) {
+      // theta_i = base^(-2 i / D); the angle in double, then rounded once
+      const double a = (double)p * pow((double)base, -2.0 * i / head_dim);
+      row[i] = (float)cos(a);
+      row[half + i] = (float)sin(a);
+    }
+  }
+  return MB_OK;
+}
+
+mb_status_t mb_rope_kv_append(void* q, void* k_cache, void* v_cache, const void* k_new,
+                              const void* v_new, const int32_t* positions,
+                              const int32_t* slot_mapping, int32_t T, const float* cos_sin,
+                              int32_t max_position, const mb_config_t* cfg, int32_t* status_dev,
+                              cudaStream_t stream) {
+  mb_status_t st = validate_config(cfg);
+  if (st != MB_OK) return st;
+  if (T < 0 || max_position <= 0) return MB_ERR_INVALID_ARG;
+  if (T == 0) return MB_OK;
+  if (!q || !k_cache || !v_cache || !k_new || !v_new || !positions || !slot_mapping || !cos_sin)
+    return MB_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) ||
+      !aligned16(v_new) || !aligned16(cos_sin) ||
+      (reinterpret_cast<uintptr_t>(positions) & 3) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 3) ||
+      (reinterpret_cast<uintptr_t>(status_dev) & 3))
+    return MB_ERR_INVALID_ARG;
+  cudaError_t e = launch_rope_append(q, k_cache, v_cache, k_new, v_new, positions, slot_mapping,
+                                     T, cfg->n_q_heads, cfg->n_kv_heads, cfg->head_dim,
+                                     cfg->page_size, cfg->num_pages, cos_sin, max_position,
+                                     status_dev, stream);
+  return e == cudaSuccess ? MB_OK : MB_ERR_CUDA;
+}
+
 mb_status_t mb_attn_forward_timed(const mb_plan_t* plan, const void* q, const void* k_cache,
                                   const void* v_cache, const int32_t* block_table_dev,
                                   void* out, float* lse, cudaStream_t stream,

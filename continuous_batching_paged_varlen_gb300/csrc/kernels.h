@@ -15,6 +15,14 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new,
                              int32_t n_kv_heads, int32_t head_dim, int32_t page_size,
                              int32_t num_pages, int32_t* status, cudaStream_t s);
 
+// Fused rotary embedding + KV append (rope_append.cu).
+cudaError_t launch_rope_append(void* q, void* k_cache, void* v_cache, const void* k_new,
+                               const void* v_new, const int32_t* positions,
+                               const int32_t* slots, int32_t T, int32_t n_q_heads,
+                               int32_t n_kv_heads, int32_t head_dim, int32_t page_size,
+                               int32_t num_pages, const float* cos_sin, int32_t max_position,
+                               int32_t* status, cudaStream_t s);
+
 // Split-KV / cascade kernel (decode.cu): partial or final rows.
 struct DecodeArgs {
   const DecodeItem* items;

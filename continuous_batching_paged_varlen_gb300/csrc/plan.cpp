@@ -585,6 +585,22 @@ mb_status_t mb_slot_mapping(const mb_request_t* reqs, int32_t n_reqs,
   return MB_OK;
 }
 
+mb_status_t mb_positions(const mb_request_t* reqs, int32_t n_reqs, int32_t* positions_out,
+                         int32_t total_q) {
+  if (n_reqs < 0 || total_q < 0) return MB_ERR_INVALID_ARG;
+  if ((n_reqs > 0 && !reqs) || (total_q > 0 && !positions_out)) return MB_ERR_INVALID_ARG;
+  for (int32_t t = 0; t < total_q; ++t) positions_out[t] = -1;
+  for (int32_t r = 0; r < n_reqs; ++r) {
+    const mb_request_t& q = reqs[r];
+    if (q.q_start < 0 || q.q_end < q.q_start || q.q_end > total_q ||
+        q.q_end - q.q_start > q.kv_length)
+      return MB_ERR_SHAPE;
+    const int32_t s0 = q.kv_length - (q.q_end - q.q_start);
+    for (int32_t t = q.q_start; t < q.q_end; ++t) positions_out[t] = s0 + (t - q.q_start);
+  }
+  return MB_OK;
+}
+
 mb_status_t mb_attn_plan_ex(const mb_request_t* reqs, int32_t n_reqs,
                             const int32_t* block_table_host,
                             const mb_config_t* cfg,

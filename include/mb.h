@@ -145,6 +145,16 @@ mb_status_t mb_slot_mapping(const mb_request_t* reqs, int32_t n_reqs,
                             const mb_config_t* cfg, int32_t* slots_out,
                             int32_t total_q);
 
+/* Host helper: the logical position of every new row (what the rotary
+ * embedding rotates by): row t of request r is at kv_length - q_rows +
+ * (t - q_start) ("ORCA and chunked prefill", section 2: kv_length counts this
+ * iteration's rows). positions_out (host, total_q entries) receives -1 for
+ * rows no request covers. Errors: MB_ERR_INVALID_ARG (null pointer, negative
+ * size), MB_ERR_SHAPE (q_start > q_end, q_rows > kv_length, a range past
+ * total_q). */
+mb_status_t mb_positions(const mb_request_t* reqs, int32_t n_reqs, int32_t* positions_out,
+                         int32_t total_q);
+
 /* KV append: scatter this iteration's K/V rows into their pages
  * ("ORCA and chunked prefill", section 4: append K, V to the cache before
  * the attention reads it). For t in [0, T): slot = slot_mapping[t];
@@ -159,6 +169,41 @@ mb_status_t mb_kv_append(void* k_cache, void* v_cache, const void* k_new,
                          const void* v_new, const int32_t* slot_mapping,
                          int32_t T, const mb_config_t* cfg, int32_t* status_dev,
                          cudaStream_t stream);
+
+/* Rotary angle table for mb_rope_kv_append (host helper, no CUDA call).
+ * cos_sin (host, max_position * head_dim floats) row p receives
+ * [cos(p theta_0) .. cos(p theta_{D/2-1}), sin(p theta_0) .. sin(p theta_{D/2-1})],
+ * theta_i = base^(-2 i / head_dim), each angle evaluated in double and rounded
+ * once to float (the rotary embedding of the Llama-2 family; the pages name
+ * the fused "norm + RoPE + write KV" kernel, "GLM-5.3 e2e token ledger",
+ * stage 6, without printing the rotation). Errors: MB_ERR_INVALID_ARG (null
+ * pointer, max_position <= 0, odd or non-positive head_dim, base <= 0). */
+mb_status_t mb_rope_table(float* cos_sin, int32_t max_position, int32_t head_dim, float base);
+
+/* Fused rotary embedding + KV append ("GLM-5.3 e2e token ledger", stage 6:
+ * RoPE and the KV write in one kernel that already holds q and k; the append
+ * of "ORCA and chunked prefill", section 4). For every token t in [0, T) at
+ * position p = positions[t]:
+ *   - each query head row q[t][h] (bf16 [T, Hq, D], device) is rotated in
+ *     place: for i < D/2 the pair (x_i, x_{i+D/2}) becomes
+ *     (x_i c - x_{i+D/2} s, x_{i+D/2} c + x_i s), c, s = cos_sin[p][i],
+ *     cos_sin[p][D/2 + i], computed in fp32 and rounded once to bf16;
+ *   - if slot = slot_mapping[t] >= 0, each KV head's k_new[t][h] is rotated
+ *     the same way into k_cache[slot / ps][h][slot % ps] and v_new[t][h] is
+ *     copied bit for bit into v_cache at the same place (k_new, v_new bf16
+ *     [T, Hkv, D], device; k_new is not modified).
+ * cos_sin: device fp32 [max_position, head_dim] (see mb_rope_table), 16-byte
+ * aligned. positions, slot_mapping: device int32 [T]. A position outside
+ * [0, max_position) skips the whole token; a slot >= num_pages * ps skips its
+ * cache write; both set bit (1 << MB_ERR_DEVICE_INDEX) in *status_dev
+ * (nullable device int32). Pages written must not be shared with another
+ * request (the caller's contract). T = 0 enqueues nothing. Asynchronous on
+ * stream; host errors as for mb_kv_append. */
+mb_status_t mb_rope_kv_append(void* q, void* k_cache, void* v_cache, const void* k_new,
+                              const void* v_new, const int32_t* positions,
+                              const int32_t* slot_mapping, int32_t T, const float* cos_sin,
+                              int32_t max_position, const mb_config_t* cfg, int32_t* status_dev,
+                              cudaStream_t stream);
 
 /* Plan one iteration. Host inputs: reqs[n_reqs] and block_table_host
  * [n_reqs, max_blocks_per_req]. Validates: config (Hq % Hkv == 0, head_dim,

@@ -7,6 +7,7 @@
   send each row's partials to one combine entry, and group shared prefixes.
 """
 
+import ctypes
 import math
 import os
 import re
@@ -21,6 +22,7 @@ from oracle import attention as OA
 from tests.conftest import ROOT, read_int_table
 
 HEADER = os.path.join(ROOT, "include", "mb.h")
+MB_ERR_INVALID_ARG, MB_ERR_SHAPE = 1, 2
 
 
 @pytest.fixture(scope="module")
@@ -233,3 +235,27 @@ def test_prefill_tiles_skip_masked_tiles(L):
     assert sorted(set((2 * (a["i0"] // 256) + 2 - a["n_kv_tiles"]).tolist())) == [0]
     # heaviest first
     assert np.all(np.diff(pitems["n_kv_tiles"]) <= 0)
+
+
+# ---------------------------------------------------------------- rotary helpers
+
+def test_rope_table_matches_oracle(L):
+    from oracle import rope as OR
+    for d, base, pmax in [(128, 10000.0, 40000), (64, 10000.0, 300), (128, 500000.0, 1000)]:
+        got = B.rope_table(pmax, d, base)
+        ref = OR.table(pmax, d, base)
+        # one rounding of an fp64 value to fp32: |err| <= 2^-24 * |value| <= 6e-8
+        np.testing.assert_allclose(got.astype(np.float64), ref, rtol=0, atol=1.2e-7)
+    out = np.empty((2, 8), np.float32)
+    assert L.mb_rope_table(out.ctypes.data, 2, 7, ctypes.c_float(10000.0)) == MB_ERR_INVALID_ARG
+    assert L.mb_rope_table(out.ctypes.data, 0, 8, ctypes.c_float(10000.0)) == MB_ERR_INVALID_ARG
+    assert L.mb_rope_table(None, 2, 8, ctypes.c_float(10000.0)) == MB_ERR_INVALID_ARG
+
+
+def test_positions_follow_the_triples(L):
+    reqs = np.array([[0, 3, 10], [3, 3, 5], [5, 6, 1], [6, 10, 4]], np.int32)
+    got = B.positions(reqs, 11)
+    np.testing.assert_array_equal(got, [7, 8, 9, -1, -1, 0, 0, 1, 2, 3, -1])
+    bad = np.array([[0, 3, 2]], np.int32)  # q_rows > kv_length
+    out = np.empty(3, np.int32)
+    assert L.mb_positions(bad.ctypes.data, 1, out.ctypes.data, 3) == MB_ERR_SHAPE
