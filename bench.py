@@ -69,6 +69,9 @@ def parse_args(argv=None):
                          "captures of the same kernels)")
     ap.add_argument("--disable-cascade", action="store_true",
                     help="plan without shared-prefix grouping (comparison runs)")
+    ap.add_argument("--rope", action="store_true",
+                    help="append through the fused rotary-embedding + KV append "
+                         "(mb_rope_kv_append) instead of the plain scatter")
     return ap.parse_args(argv)
 
 
@@ -310,6 +313,8 @@ def workload_config_args(w, args):
         c["max_requests"] = args.max_requests
     if args.disable_cascade:
         c["cascade"] = "disabled"
+    if args.rope:
+        c["append"] = "fused rotary embedding + KV append (mb_rope_kv_append)"
     return c
 
 
@@ -346,6 +351,11 @@ def run_gpu(args):
         hs = B.slot_mapping(w.hist_requests, w.block_table, cfg, n_hist)
         B.kv_append(kc, vc, w.k_hist, w.v_hist, torch.from_numpy(hs).to(dev), cfg, status)
     slots = torch.from_numpy(B.slot_mapping(w.requests, w.block_table, cfg, w.total_q)).to(dev)
+    if args.rope:
+        pos_dev = torch.from_numpy(B.positions(w.requests, w.total_q)).to(dev)
+        rope_tab = torch.from_numpy(
+            B.rope_table(int(w.requests[:, 2].max()) + 1, s.head_dim)).to(dev)
+        q_rot = w.q.clone()  # rotated in place every step (timing only)
     bt_dev = torch.from_numpy(np.ascontiguousarray(w.block_table)).to(dev)
     q, k_new, v_new = w.q, w.k_new, w.v_new
     out = torch.empty((w.total_q, s.n_q_heads, s.head_dim), dtype=torch.bfloat16, device=dev)
@@ -358,14 +368,23 @@ def run_gpu(args):
     probe.close()
     launches_per_step = 1 + info["n_launches"]
 
+    def append():
+        if args.rope:
+            B.rope_kv_append(q_rot, kc, vc, k_new, v_new, pos_dev, slots, rope_tab, cfg, status)
+        else:
+            B.kv_append(kc, vc, k_new, v_new, slots, cfg, status)
+
     def step(stage_events=None):
-        B.kv_append(kc, vc, k_new, v_new, slots, cfg, status)
+        append()
         plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=ws, opts=opts)
         plan.forward(q, kc, vc, bt_dev, out, lse, events=stage_events)
         plan.close()
 
-    def kernel_pass(stage_events):
+    def kernel_pass(stage_events, append_events):
         # the same launches with per-stage events (stages back to back)
+        append_events[0].record(stream)
+        append()
+        append_events[1].record(stream)
         plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=ws, opts=opts)
         plan.forward(q, kc, vc, bt_dev, out, lse, events=stage_events)
         plan.close()
@@ -379,6 +398,8 @@ def run_gpu(args):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
     sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(STAGES))]
+           for _ in range(K)]
+    aev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(K)]
     for row in sev:  # torch creates the CUDA event on first record: do it here so the
         for e in row:  # library receives real handles
@@ -420,7 +441,7 @@ def run_gpu(args):
     # stage bracketed by its own events (L2 flushed before every pass)
     for i in range(K):
         flush.zero_()
-        kernel_pass(sev[i])
+        kernel_pass(sev[i], aev[i])
     torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     stage_ms = {}
@@ -429,6 +450,7 @@ def run_gpu(args):
                  "prefill": "n_prefill_items"}[name]] > 0:
             stage_ms[name] = statistics.mean(
                 sev[i][2 * si].elapsed_time(sev[i][2 * si + 1]) for i in range(K))
+    stage_ms["append"] = statistics.mean(a.elapsed_time(b) for a, b in aev)
     ms_step = statistics.mean(step_ms)
     total_ms = sum(step_ms)
     if world > 1:
@@ -441,6 +463,9 @@ def run_gpu(args):
     # ---- roofline of the dominant kernel
     peaks = load_peaks()
     work = stage_work(w)
+    if args.rope:
+        work["append_bytes"] = C.rope_append_bytes(w.total_q, s.n_q_heads, s.n_kv_heads,
+                                                   s.head_dim)
     dominant = max(stage_ms, key=stage_ms.get) if stage_ms else None
     roof = None
     if dominant == "prefill":
@@ -452,6 +477,13 @@ def run_gpu(args):
                 "peak_kind": f"bf16 dense burst ({peaks['source']})",
                 "algorithmic_per_launch": work["prefill_flops"],
                 "traffic": recorded_traffic("prefill", s.name)}
+    elif dominant == "append":
+        t = stage_ms["append"] / 1e3
+        ach = work["append_bytes"] / t / 1e9
+        roof = {"kernel": "rope_append_kernel" if args.rope else "kv_append_kernel",
+                "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "peak_kind": f"HBM copy ({peaks['source']})",
+                "algorithmic_per_launch": work["append_bytes"], "traffic": None}
     elif dominant == "decode":
         t = stage_ms["decode"] / 1e3
         ach = work["decode_bytes"] / t / 1e9
@@ -520,7 +552,8 @@ def run_gpu(args):
         "achieved": {"attention_tflops": work["total_flops"] / (ms_step / 1e3) / 1e12,
                      "attention_hbm_gbs": work["total_bytes"] / (ms_step / 1e3) / 1e9,
                      "algorithmic_flops_per_step": work["total_flops"],
-                     "algorithmic_bytes_per_step": work["total_bytes"] + work["append_bytes"]},
+                     "algorithmic_bytes_per_step": work["total_bytes"] + work["append_bytes"],
+                     "append_hbm_gbs": work["append_bytes"] / (stage_ms["append"] / 1e3) / 1e9},
         "plan": info, "device_status": dev_status, "wall_s_timed_region": wall,
         # host time to enqueue one step (append, plan + upload, forward, through
         # the Python binding); a step shorter than this on the device is

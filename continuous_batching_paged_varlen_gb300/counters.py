@@ -77,3 +77,13 @@ def append_bytes(n_new_tokens: int, n_kv_heads: int, head_dim: int,
                  elem_bytes: int = 2) -> int:
     """Read the new K and V rows and write them into the cache, + slots."""
     return 2 * 2 * n_new_tokens * n_kv_heads * head_dim * elem_bytes + 4 * n_new_tokens
+
+
+def rope_append_bytes(n_new_tokens: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                      elem_bytes: int = 2) -> int:
+    """Fused rotary embedding + append: read and write every query row (rotated
+    in place), read K and V and write them into the cache, read the token's
+    angle-table row (fp32) and its position and slot."""
+    per_token = (2 * n_q_heads * head_dim * elem_bytes + 4 * n_kv_heads * head_dim * elem_bytes
+                 + head_dim * 4 + 8)
+    return n_new_tokens * per_token

@@ -10,11 +10,11 @@
 // the one of "ORCA and chunked prefill", section 4 (slot per new row from the
 // host, "GLM-5.3 e2e token ledger", stage 4).
 //
-// One block per token, one warp per head row at a time: lane l owns D/64
-// consecutive elements of the first half and the matching elements of the
-// second half, computes the rotation in fp32 and rounds once to bf16. Q rows
-// are rotated in place; K rows are rotated into their cache slot; V rows are
-// copied bit for bit (16-byte chunks).
+// One block per token; a thread rotates one 16-byte unit at a time (8
+// elements of a row's first half and the matching 8 of its second half, with
+// their 8 angles), in fp32, rounded once to bf16. Q rows are rotated in place;
+// K rows are rotated into their cache slot; V rows are copied bit for bit
+// (16-byte chunks).
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -25,16 +25,33 @@
 namespace mb {
 namespace {
 
+constexpr int kThreads = 128;
+
+// 8 bf16 (one 16-byte chunk) <-> 8 floats
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    f[2 * k] = dev::bf16_lo(w[k]);
+    f[2 * k + 1] = dev::bf16_hi(w[k]);
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(dev::pack_bf16x2(f[0], f[1]), dev::pack_bf16x2(f[2], f[3]),
+                    dev::pack_bf16x2(f[4], f[5]), dev::pack_bf16x2(f[6], f[7]));
+}
+
 template <int D>
-__global__ void __launch_bounds__(128) rope_append_kernel(
+__global__ void __launch_bounds__(kThreads) rope_append_kernel(
     __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ kc, uint4* __restrict__ vc,
     const __nv_bfloat16* __restrict__ kn, const uint4* __restrict__ vn,
     const int32_t* __restrict__ positions, const int32_t* __restrict__ slots, int32_t Hq,
     int32_t Hkv, int32_t ps_shift, int64_t n_slots, const float* __restrict__ cos_sin,
     int32_t max_position, int32_t* status) {
   constexpr int HALF = D / 2;
+  constexpr int RU = D / 16;  // rotation units per row: 8 elements of each half
+  constexpr int CH = D / 8;   // 16-byte chunks per row
   const int t = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t pos = __ldg(positions + t);
   if (pos < 0 || pos >= max_position) {
     if (threadIdx.x == 0) dev::set_status(status, MB_ERR_DEVICE_INDEX);
@@ -45,54 +62,49 @@ __global__ void __launch_bounds__(128) rope_append_kernel(
     if (threadIdx.x == 0) dev::set_status(status, MB_ERR_DEVICE_INDEX);
     slot = -1;
   }
-  // lane l owns elements [E l, E l + E) of each half (E = D / 64: one bf16
-  // pair for D = 128, one element for D = 64) and their angles
-  constexpr int E = D / 64;
-  float c[E], s[E];
-  const float* row = cos_sin + (int64_t)pos * D + E * lane;
-#pragma unroll
-  for (int k = 0; k < E; ++k) {
-    c[k] = __ldg(row + k);
-    s[k] = __ldg(row + HALF + k);
-  }
-  auto rotate_row = [&](const __nv_bfloat16* src, __nv_bfloat16* dst) {
-    float x[E], y[E];
-    if constexpr (E == 2) {
-      const uint32_t lo = *reinterpret_cast<const uint32_t*>(src + 2 * lane);
-      const uint32_t hi = *reinterpret_cast<const uint32_t*>(src + HALF + 2 * lane);
-      x[0] = dev::bf16_lo(lo);
-      x[1] = dev::bf16_hi(lo);
-      y[0] = dev::bf16_lo(hi);
-      y[1] = dev::bf16_hi(hi);
-      *reinterpret_cast<uint32_t*>(dst + 2 * lane) =
-          dev::pack_bf16x2(fmaf(x[0], c[0], -y[0] * s[0]), fmaf(x[1], c[1], -y[1] * s[1]));
-      *reinterpret_cast<uint32_t*>(dst + HALF + 2 * lane) =
-          dev::pack_bf16x2(fmaf(y[0], c[0], x[0] * s[0]), fmaf(y[1], c[1], x[1] * s[1]));
+  const bool write_kv = slot >= 0;
+  const int32_t page = write_kv ? slot >> ps_shift : 0;
+  const int32_t off = write_kv ? slot & ((1 << ps_shift) - 1) : 0;
+  const int64_t cache_base = (((int64_t)page * Hkv) << ps_shift) + off;  // head 0's page row
+  const float* row = cos_sin + (int64_t)pos * D;
+  // query rows (rotated in place), then K rows (rotated into the cache)
+  const int n_rot = (Hq + (write_kv ? Hkv : 0)) * RU;
+  for (int i = threadIdx.x; i < n_rot; i += kThreads) {
+    const int r = i / RU, u = i - r * RU;
+    const __nv_bfloat16* src;
+    __nv_bfloat16* dst;
+    if (r < Hq) {
+      src = dst = q + ((int64_t)t * Hq + r) * D;
     } else {
-      x[0] = __bfloat162float(src[lane]);
-      y[0] = __bfloat162float(src[HALF + lane]);
-      dst[lane] = __float2bfloat16_rn(fmaf(x[0], c[0], -y[0] * s[0]));
-      dst[HALF + lane] = __float2bfloat16_rn(fmaf(y[0], c[0], x[0] * s[0]));
+      const int h = r - Hq;
+      src = kn + ((int64_t)t * Hkv + h) * D;
+      dst = kc + (cache_base + ((int64_t)h << ps_shift)) * D;
     }
-  };
-  // query rows, in place
-  for (int h = warp; h < Hq; h += 4) {
-    __nv_bfloat16* r = q + ((int64_t)t * Hq + h) * D;
-    rotate_row(r, r);
+    const uint4 lo_v = *reinterpret_cast<const uint4*>(src + 8 * u);
+    const uint4 hi_v = *reinterpret_cast<const uint4*>(src + HALF + 8 * u);
+    const float4 c0 = __ldg(reinterpret_cast<const float4*>(row + 8 * u));
+    const float4 c1 = __ldg(reinterpret_cast<const float4*>(row + 8 * u + 4));
+    const float4 s0 = __ldg(reinterpret_cast<const float4*>(row + HALF + 8 * u));
+    const float4 s1 = __ldg(reinterpret_cast<const float4*>(row + HALF + 8 * u + 4));
+    const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    float x[8], y[8], xo[8], yo[8];
+    unpack8(lo_v, x);
+    unpack8(hi_v, y);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      xo[e] = fmaf(x[e], c[e], -y[e] * sn[e]);
+      yo[e] = fmaf(y[e], c[e], x[e] * sn[e]);
+    }
+    *reinterpret_cast<uint4*>(dst + 8 * u) = pack8(xo);
+    *reinterpret_cast<uint4*>(dst + HALF + 8 * u) = pack8(yo);
   }
-  if (slot < 0) return;  // padding row (or flagged): no cache write
-  const int32_t page = slot >> ps_shift;
-  const int32_t off = slot & ((1 << ps_shift) - 1);
-  for (int h = warp; h < Hkv; h += 4) {
-    const int64_t dst_row = (((int64_t)page * Hkv + h) << ps_shift) + off;
-    rotate_row(kn + ((int64_t)t * Hkv + h) * D, kc + dst_row * D);
-  }
+  if (!write_kv) return;  // padding row (or flagged): no cache write
   // V: plain copy, 16-byte chunks
-  constexpr int CH = D / 8;
-  for (int i = threadIdx.x; i < Hkv * CH; i += blockDim.x) {
-    const int h = i / CH, cidx = i - h * CH;
-    const int64_t dst_row = (((int64_t)page * Hkv + h) << ps_shift) + off;
-    vc[dst_row * CH + cidx] = __ldg(vn + ((int64_t)t * Hkv + h) * CH + cidx);
+  const uint4* vsrc = vn + (int64_t)t * Hkv * CH;
+  for (int c = threadIdx.x; c < Hkv * CH; c += kThreads) {
+    const int h = c / CH, cc = c - h * CH;
+    vc[(cache_base + ((int64_t)h << ps_shift)) * CH + cc] = __ldg(vsrc + c);
   }
 }
 
@@ -107,12 +119,12 @@ cudaError_t launch_rope_append(void* q, void* k_cache, void* v_cache, const void
   const int ps_shift = __builtin_ctz((unsigned)page_size);
   const int64_t n_slots = (int64_t)num_pages * page_size;
   if (head_dim == 128)
-    rope_append_kernel<128><<<(unsigned)T, 128, 0, s>>>(
+    rope_append_kernel<128><<<(unsigned)T, kThreads, 0, s>>>(
         (__nv_bfloat16*)q, (__nv_bfloat16*)k_cache, (uint4*)v_cache,
         (const __nv_bfloat16*)k_new, (const uint4*)v_new, positions, slots, n_q_heads,
         n_kv_heads, ps_shift, n_slots, cos_sin, max_position, status);
   else
-    rope_append_kernel<64><<<(unsigned)T, 128, 0, s>>>(
+    rope_append_kernel<64><<<(unsigned)T, kThreads, 0, s>>>(
         (__nv_bfloat16*)q, (__nv_bfloat16*)k_cache, (uint4*)v_cache,
         (const __nv_bfloat16*)k_new, (const uint4*)v_new, positions, slots, n_q_heads,
         n_kv_heads, ps_shift, n_slots, cos_sin, max_position, status);
