@@ -61,6 +61,23 @@ class PlanInfo(ctypes.Structure):
         return {k: getattr(self, k) for k, _ in self._fields_}
 
 
+class SchedConfig(ctypes.Structure):
+    _fields_ = [("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("max_blocks_per_req", ctypes.c_int32), ("token_budget", ctypes.c_int32),
+                ("max_running", ctypes.c_int32), ("decode_rows", ctypes.c_int32)]
+
+
+class SchedStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("n_reqs", "total_q", "n_prefill", "n_decode", "n_preempted", "n_prefix_hits",
+                 "n_waiting", "n_running", "n_finished", "free_pages")]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+SCHED_STATES = {0: "waiting", 1: "prefill", 2: "decode", 3: "finished"}
+
 _lib = None
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -115,6 +132,21 @@ def lib():
     L.mb_attn_destroy.argtypes = [_vp]
     L.mb_attn_forward_noalloc.restype = ctypes.c_int
     L.mb_attn_forward_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    L.mb_sched_create.restype = ctypes.c_int
+    L.mb_sched_create.argtypes = [ctypes.POINTER(SchedConfig), ctypes.POINTER(_vp)]
+    L.mb_sched_destroy.restype = ctypes.c_int
+    L.mb_sched_destroy.argtypes = [_vp]
+    L.mb_sched_add.restype = ctypes.c_int
+    L.mb_sched_add.argtypes = [_vp, _i32, _i32, _i32, _i32, _pi32]
+    L.mb_sched_step.restype = ctypes.c_int
+    L.mb_sched_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32,
+                                ctypes.POINTER(SchedStats)]
+    L.mb_sched_commit.restype = ctypes.c_int
+    L.mb_sched_commit.argtypes = [_vp, _vp, _i32, _pi32]
+    L.mb_sched_page_refs.restype = ctypes.c_int
+    L.mb_sched_page_refs.argtypes = [_vp, _vp, _i32]
+    L.mb_sched_request_info.restype = ctypes.c_int
+    L.mb_sched_request_info.argtypes = [_vp, _i32, _vp]
     _lib = L
     return L
 
@@ -311,6 +343,89 @@ class Plan:
     def close(self):
         if getattr(self, "_h", None):
             lib().mb_attn_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Iteration:
+    """One built iteration of ``Scheduler.step``: host arrays shaped for the
+    library's calls (``requests`` [n, 3] triples, ``ids`` [n], ``block_table``
+    [n, max_blocks], ``slots`` and ``positions`` [total_q]) and the counters."""
+
+    def __init__(self, requests, ids, block_table, slots, positions, stats):
+        self.requests, self.ids, self.block_table = requests, ids, block_table
+        self.slots, self.positions, self.stats = slots, positions, stats
+
+    @property
+    def total_q(self) -> int:
+        return int(self.stats["total_q"])
+
+
+class Scheduler:
+    """The host iteration builder of ``include/mb_sched.h`` (``mb_sched_*``)."""
+
+    def __init__(self, num_pages, page_size, max_blocks_per_req, token_budget, max_running=0,
+                 decode_rows=1):
+        self.cfg = SchedConfig(num_pages, page_size, max_blocks_per_req, token_budget,
+                               max_running, decode_rows)
+        h = _vp()
+        check(lib().mb_sched_create(ctypes.byref(self.cfg), ctypes.byref(h)), "mb_sched_create")
+        self._h = h
+        self.n_added = 0
+
+    def add(self, prompt_len, max_new_tokens, prefix_id=-1, prefix_len=0) -> int:
+        rid = ctypes.c_int32()
+        check(lib().mb_sched_add(self._h, prompt_len, max_new_tokens, prefix_id, prefix_len,
+                                 ctypes.byref(rid)), "mb_sched_add")
+        self.n_added += 1
+        return int(rid.value)
+
+    def step(self) -> Iteration:
+        cap_r = max(1, self.n_added)
+        cap_q = max(1, self.cfg.token_budget)
+        mb = self.cfg.max_blocks_per_req
+        reqs = np.zeros((cap_r, 3), np.int32)
+        ids = np.zeros(cap_r, np.int32)
+        bt = np.zeros((cap_r, mb), np.int32)
+        slots = np.zeros(cap_q, np.int32)
+        pos = np.zeros(cap_q, np.int32)
+        st = SchedStats()
+        check(lib().mb_sched_step(self._h, reqs.ctypes.data, ids.ctypes.data, bt.ctypes.data,
+                                  slots.ctypes.data, pos.ctypes.data, cap_r, cap_q,
+                                  ctypes.byref(st)), "mb_sched_step")
+        n, q = st.n_reqs, st.total_q
+        return Iteration(reqs[:n].copy(), ids[:n].copy(), bt[:n].copy(), slots[:q].copy(),
+                         pos[:q].copy(), st.as_dict())
+
+    def commit(self) -> list:
+        out = np.zeros(max(1, self.n_added), np.int32)
+        n = ctypes.c_int32()
+        check(lib().mb_sched_commit(self._h, out.ctypes.data, out.size, ctypes.byref(n)),
+              "mb_sched_commit")
+        return out[:n.value].tolist()
+
+    def page_refs(self) -> np.ndarray:
+        out = np.zeros(self.cfg.num_pages, np.int32)
+        check(lib().mb_sched_page_refs(self._h, out.ctypes.data, out.size), "mb_sched_page_refs")
+        return out
+
+    def request_info(self, rid) -> dict:
+        out = np.zeros(8, np.int32)
+        check(lib().mb_sched_request_info(self._h, rid, out.ctypes.data), "mb_sched_request_info")
+        keys = ("state", "computed", "generated", "pages", "preemptions", "prompt_len",
+                "max_new_tokens", "prefix_id")
+        d = dict(zip(keys, out.tolist()))
+        d["state"] = SCHED_STATES[d["state"]]
+        return d
+
+    def close(self):
+        if self._h:
+            lib().mb_sched_destroy(self._h)
             self._h = None
 
     def __del__(self):

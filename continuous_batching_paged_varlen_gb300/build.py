@@ -18,8 +18,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmb.so")
-SOURCES = ["plan.cpp", "api.cu", "kv_append.cu", "rope_append.cu", "decode.cu", "combine.cu",
-           "prefill.cu", "noalloc.cu"]
+SOURCES = ["plan.cpp", "sched.cpp", "api.cu", "kv_append.cu", "rope_append.cu", "decode.cu",
+           "combine.cu", "prefill.cu", "noalloc.cu"]
 HEADERS = ["mb_internal.h", "mb_device.cuh", "kernels.h", "plan_impl.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -35,7 +35,8 @@ def nvcc() -> str:
 
 def _inputs():
     return ([os.path.join(CSRC, s) for s in SOURCES + HEADERS]
-            + [os.path.join(ROOT, "include", "mb.h"), os.path.abspath(__file__)])
+            + [os.path.join(ROOT, "include", h) for h in ("mb.h", "mb_sched.h")]
+            + [os.path.abspath(__file__)])
 
 
 def up_to_date() -> bool:

@@ -32,7 +32,9 @@ def L():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    inc = os.path.join(ROOT, "include")
+    text = "\n".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc))
+                     if f.endswith(".h"))
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(mb_[a-z0-9_]+)\s*\(", text)))
 
