@@ -18,10 +18,14 @@ brute
 rope
     The rotary embedding fused into the KV append (rotate-half pairs at the
     token's position, the fp64 angle table) and the fused append itself.
+fp8
+    The e4m3 codec from the format's definition, per-row quantization with
+    fp32 scales, the fp8 append; attention over an fp8 cache is ``attention``
+    on the dequantized values.
 
 Every function is pinned by ``tests/test_oracle.py`` (worked example,
 special cases reducing to library routines, closed forms, invariants and
 brute force). No function is unpinned.
 """
 
-from . import attention, brute, rope  # noqa: F401
+from . import attention, brute, fp8, rope  # noqa: F401
