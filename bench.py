@@ -48,7 +48,8 @@ DEFAULT_WORKLOAD = "llama2_7b_orca_iteration"
 PREFILL_MIN_ROWS = 16  # the planner's default split between the two kernels
 FLUSH_BYTES = 256 << 20
 STAGES = ["decode", "combine", "prefill"]
-KERNEL_SOURCES = {"prefill": "prefill.cu", "decode": "decode.cu", "combine": "combine.cu"}
+KERNEL_SOURCES = {"prefill": "prefill.cu", "decode": "decode.cu", "combine": "combine.cu",
+                  "decode_fp8": "decode_fp8.cu"}
 
 
 def parse_args(argv=None):
@@ -72,7 +73,14 @@ def parse_args(argv=None):
     ap.add_argument("--rope", action="store_true",
                     help="append through the fused rotary-embedding + KV append "
                          "(mb_rope_kv_append) instead of the plain scatter")
-    return ap.parse_args(argv)
+    ap.add_argument("--fp8", action="store_true",
+                    help="fp8 (e4m3) KV cache with per-row fp32 scales: quantizing append "
+                         "(mb_kv_append_fp8) and mb_attn_forward_fp8 (every request on the "
+                         "split-KV path)")
+    args = ap.parse_args(argv)
+    if args.fp8 and args.rope:
+        ap.error("--fp8 and --rope are separate variants")
+    return args
 
 
 def dist_env():
@@ -97,27 +105,31 @@ def load_peaks():
 
 # --------------------------------------------------------------- algorithmic work
 
-def stage_work(w):
-    """Algorithmic FLOPs and bytes of the two attention kernels' request sets."""
+def stage_work(w, fp8=False):
+    """Algorithmic FLOPs and bytes of the two attention kernels' request sets
+    (fp8: every request on the split-KV kernel, 1-byte K/V + fp32 row scales)."""
     s = w.spec
     reqs = w.requests
     m = reqs[:, 1] - reqs[:, 0]
-    pre = reqs[m >= PREFILL_MIN_ROWS]
-    dec_idx = np.nonzero((m > 0) & (m < PREFILL_MIN_ROWS))[0]
+    split_min = (1 << 30) if fp8 else PREFILL_MIN_ROWS
+    kvb = dict(kv_elem_bytes=1, kv_row_scale_bytes=4) if fp8 else {}
+    pre = reqs[m >= split_min]
+    dec_idx = np.nonzero((m > 0) & (m < split_min))[0]
     dec = reqs[dec_idx]
     out = {}
     out["prefill_flops"] = C.attention_flops(pre, s.n_q_heads, s.head_dim) if len(pre) else 0
-    out["prefill_bytes"] = (C.attention_bytes(pre, w.block_table[m >= PREFILL_MIN_ROWS],
+    out["prefill_bytes"] = (C.attention_bytes(pre, w.block_table[m >= split_min],
                                               s.n_q_heads, s.n_kv_heads, s.head_dim,
-                                              s.page_size) if len(pre) else 0)
+                                              s.page_size, **kvb) if len(pre) else 0)
     out["decode_flops"] = C.attention_flops(dec, s.n_q_heads, s.head_dim) if len(dec) else 0
     out["decode_bytes"] = (C.attention_bytes(dec, w.block_table[dec_idx], s.n_q_heads,
-                                             s.n_kv_heads, s.head_dim, s.page_size)
+                                             s.n_kv_heads, s.head_dim, s.page_size, **kvb)
                            if len(dec) else 0)
     out["total_flops"] = C.attention_flops(reqs, s.n_q_heads, s.head_dim)
     out["total_bytes"] = C.attention_bytes(reqs, w.block_table, s.n_q_heads, s.n_kv_heads,
-                                           s.head_dim, s.page_size)
-    out["append_bytes"] = C.append_bytes(w.total_q, s.n_kv_heads, s.head_dim)
+                                           s.head_dim, s.page_size, **kvb)
+    out["append_bytes"] = (C.append_fp8_bytes(w.total_q, s.n_kv_heads, s.head_dim) if fp8
+                           else C.append_bytes(w.total_q, s.n_kv_heads, s.head_dim))
     return out
 
 
@@ -202,10 +214,13 @@ class ClockSampler:
 
 # --------------------------------------------------------------- CPU oracle timing
 
-def time_oracle_sample(w, budget_s, rotate=0):
+def time_oracle_sample(w, budget_s, rotate=0, fp8=False):
     """Time the fp64 oracle on a bounded sample of workload w; returns
-    (Q rows/s extrapolated to the whole workload, description, seconds)."""
+    (Q rows/s extrapolated to the whole workload, description, seconds).
+    fp8: each request's K/V go through the oracle's e4m3 quantization and
+    dequantization first (timed with the request's first head)."""
     from oracle import attention as OA  # the oracle is only used on this leg
+    from oracle import fp8 as OF
 
     s = w.spec
     g = s.n_q_heads // s.n_kv_heads
@@ -218,11 +233,17 @@ def time_oracle_sample(w, budget_s, rotate=0):
         if qe == qs:
             continue
         k, v = w.logical_kv(r)
-        k = k.to("cpu").double().numpy()
-        v = v.to("cpu").double().numpy()
+        t0 = time.perf_counter()
+        if fp8:
+            k = OF.dequantize_rows(*OF.quantize_rows(k.to("cpu").float().numpy()))
+            v = OF.dequantize_rows(*OF.quantize_rows(v.to("cpu").float().numpy()))
+        else:
+            k = k.to("cpu").double().numpy()
+            v = v.to("cpu").double().numpy()
         q = w.q[qs:qe].to("cpu").double().numpy()
         heads_done = 0
-        t_req = 0.0
+        t_req = (time.perf_counter() - t0) if fp8 else 0.0
+        spent += t_req
         for i in range(s.n_q_heads):
             h = (i + rotate) % s.n_q_heads
             kh = h // g
@@ -267,7 +288,7 @@ def run_reference(args):
     rates = []
     desc = ""
     for i in range(args.warmup + args.steps):
-        rate, desc, spent = time_oracle_sample(w, per_step, rotate=i)
+        rate, desc, spent = time_oracle_sample(w, per_step, rotate=i, fp8=args.fp8)
         if i >= args.warmup:
             rates.append(rate)
     value = statistics.median(rates)
@@ -275,7 +296,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.total_q / value * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(w),
+        "data": "synthetic", "config": workload_config_args(w, args),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                          "sample": f"per step ~{per_step:.0f} s of fp64 oracle work: {desc}; "
                                    "rate extrapolated to every head / request"},
@@ -315,6 +336,11 @@ def workload_config_args(w, args):
         c["cascade"] = "disabled"
     if args.rope:
         c["append"] = "fused rotary embedding + KV append (mb_rope_kv_append)"
+    if args.fp8:
+        c["kv_cache"] = ("fp8 e4m3 codes + one fp32 scale per (token, KV head) row; "
+                         "mb_kv_append_fp8 + mb_attn_forward_fp8, every request on the "
+                         "split-KV kernel")
+        c["step"] = "mb_kv_append_fp8 + mb_attn_plan (host + 1 H2D) + mb_attn_forward_fp8"
     return c
 
 
@@ -339,17 +365,39 @@ def run_gpu(args):
     if args.max_requests:
         w = truncate(w, args.max_requests)
     s = w.spec
-    opts = B.options(disable_cascade=1) if args.disable_cascade else None
+    opts = None
+    if args.disable_cascade or args.fp8:
+        opts = B.options(disable_cascade=1 if args.disable_cascade else 0,
+                         prefill_min_rows=-1 if args.fp8 else 0)
     cfg = B.config(s.n_q_heads, s.n_kv_heads, s.head_dim, s.page_size, w.num_pages,
                    w.block_table.shape[1], s.scale or 0.0)
     shape = (w.num_pages, s.n_kv_heads, s.page_size, s.head_dim)
-    kc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
-    vc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if args.fp8:
+        kc = torch.zeros(shape, dtype=torch.uint8, device=dev)    # e4m3 codes
+        vc = torch.zeros(shape, dtype=torch.uint8, device=dev)
+        ksc = torch.zeros(shape[:3], dtype=torch.float32, device=dev)
+        vsc = torch.zeros(shape[:3], dtype=torch.float32, device=dev)
+    else:
+        kc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+        vc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+
+    def append_rows(kn, vn, slot_t):
+        if args.fp8:
+            B.kv_append_fp8(kc, vc, ksc, vsc, kn, vn, slot_t, cfg, status)
+        else:
+            B.kv_append(kc, vc, kn, vn, slot_t, cfg, status)
+
+    def forward(plan, q_t, events=None):
+        if args.fp8:
+            plan.forward_fp8(q_t, kc, vc, ksc, vsc, bt_dev, out, lse, events=events)
+        else:
+            plan.forward(q_t, kc, vc, bt_dev, out, lse, events=events)
+
     n_hist = int(w.hist_requests[:, 1].max()) if w.n_requests else 0
     if n_hist:
         hs = B.slot_mapping(w.hist_requests, w.block_table, cfg, n_hist)
-        B.kv_append(kc, vc, w.k_hist, w.v_hist, torch.from_numpy(hs).to(dev), cfg, status)
+        append_rows(w.k_hist, w.v_hist, torch.from_numpy(hs).to(dev))
     slots = torch.from_numpy(B.slot_mapping(w.requests, w.block_table, cfg, w.total_q)).to(dev)
     if args.rope:
         pos_dev = torch.from_numpy(B.positions(w.requests, w.total_q)).to(dev)
@@ -372,12 +420,12 @@ def run_gpu(args):
         if args.rope:
             B.rope_kv_append(q_rot, kc, vc, k_new, v_new, pos_dev, slots, rope_tab, cfg, status)
         else:
-            B.kv_append(kc, vc, k_new, v_new, slots, cfg, status)
+            append_rows(k_new, v_new, slots)
 
     def step(stage_events=None):
         append()
         plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=ws, opts=opts)
-        plan.forward(q, kc, vc, bt_dev, out, lse, events=stage_events)
+        forward(plan, q, stage_events)
         plan.close()
 
     def kernel_pass(stage_events, append_events):
@@ -386,7 +434,7 @@ def run_gpu(args):
         append()
         append_events[1].record(stream)
         plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=ws, opts=opts)
-        plan.forward(q, kc, vc, bt_dev, out, lse, events=stage_events)
+        forward(plan, q, stage_events)
         plan.close()
 
     for _ in range(args.warmup):
@@ -462,7 +510,7 @@ def run_gpu(args):
 
     # ---- roofline of the dominant kernel
     peaks = load_peaks()
-    work = stage_work(w)
+    work = stage_work(w, fp8=args.fp8)
     if args.rope:
         work["append_bytes"] = C.rope_append_bytes(w.total_q, s.n_q_heads, s.n_kv_heads,
                                                    s.head_dim)
@@ -480,18 +528,20 @@ def run_gpu(args):
     elif dominant == "append":
         t = stage_ms["append"] / 1e3
         ach = work["append_bytes"] / t / 1e9
-        roof = {"kernel": "rope_append_kernel" if args.rope else "kv_append_kernel",
+        roof = {"kernel": ("rope_append_kernel" if args.rope else
+                           "kv_append_fp8_kernel" if args.fp8 else "kv_append_kernel"),
                 "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / peaks["hbm_gbs"], "peak_kind": f"HBM copy ({peaks['source']})",
                 "algorithmic_per_launch": work["append_bytes"], "traffic": None}
     elif dominant == "decode":
         t = stage_ms["decode"] / 1e3
         ach = work["decode_bytes"] / t / 1e9
-        roof = {"kernel": "splitkv_kernel", "bound": "hbm", "achieved": ach,
+        roof = {"kernel": "splitkv_fp8_kernel" if args.fp8 else "splitkv_kernel",
+                "bound": "hbm", "achieved": ach,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
                 "peak_kind": f"HBM copy ({peaks['source']})",
                 "algorithmic_per_launch": work["decode_bytes"],
-                "traffic": recorded_traffic("decode", s.name)}
+                "traffic": recorded_traffic("decode_fp8" if args.fp8 else "decode", s.name)}
 
     # ---- end to end through host buffers
     e2e = None
@@ -507,9 +557,9 @@ def run_gpu(args):
             dq.copy_(hq, non_blocking=True)
             dk.copy_(hk, non_blocking=True)
             dv.copy_(hv, non_blocking=True)
-            B.kv_append(kc, vc, dk, dv, slots, cfg, status)
+            append_rows(dk, dv, slots)
             plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=ws, opts=opts)
-            plan.forward(dq, kc, vc, bt_dev, out, lse)
+            forward(plan, dq)
             plan.close()
             hout.copy_(out, non_blocking=True)
             hlse.copy_(lse, non_blocking=True)
@@ -535,7 +585,7 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, desc, spent = time_oracle_sample(w, args.cpu_seconds)
+        rate, desc, spent = time_oracle_sample(w, args.cpu_seconds, fp8=args.fp8)
         cpu = {"value": rate, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                "sample": f"{spent:.1f} s of fp64 oracle work: {desc}; extrapolated to every "
                          "head / request of the workload"}
@@ -543,7 +593,8 @@ def run_gpu(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 KV + bf16" if args.fp8 else "bf16", "data": "synthetic",
         "config": {**workload_config_args(w, args), "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * K,

@@ -101,6 +101,13 @@ def lib():
     L.mb_slot_mapping.argtypes = [_vp, _i32, _vp, ctypes.POINTER(Config), _vp, _i32]
     L.mb_kv_append.restype = ctypes.c_int
     L.mb_kv_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, ctypes.POINTER(Config), _vp, _vp]
+    L.mb_kv_append_fp8.restype = ctypes.c_int
+    L.mb_kv_append_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                   ctypes.POINTER(Config), _vp, _vp]
+    L.mb_attn_forward_fp8.restype = ctypes.c_int
+    L.mb_attn_forward_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    L.mb_attn_forward_fp8_timed.restype = ctypes.c_int
+    L.mb_attn_forward_fp8_timed.argtypes = [_vp] * 11
     L.mb_positions.restype = ctypes.c_int
     L.mb_positions.argtypes = [_vp, _i32, _vp, _i32]
     L.mb_rope_table.restype = ctypes.c_int
@@ -215,6 +222,18 @@ def rope_table(max_position: int, head_dim: int, base: float = 10000.0) -> np.nd
     check(lib().mb_rope_table(out.ctypes.data, max_position, head_dim, float(base)),
           "mb_rope_table")
     return out
+
+
+def kv_append_fp8(k_codes, v_codes, k_scale, v_scale, k_new, v_new, slots, cfg: Config,
+                  status=None, stream=None):
+    """``mb_kv_append_fp8`` on torch tensors: quantizes each (token, KV head)
+    row of ``k_new`` / ``v_new`` (bf16) into the e4m3 code caches (uint8) and
+    their fp32 per-row scales."""
+    T = int(slots.numel())
+    check(lib().mb_kv_append_fp8(_ptr(k_codes), _ptr(v_codes), _ptr(k_scale), _ptr(v_scale),
+                                 _ptr(k_new), _ptr(v_new), _ptr(slots), T, ctypes.byref(cfg),
+                                 _ptr(status), _stream_ptr(stream) if T else None),
+          "mb_kv_append_fp8")
 
 
 def rope_kv_append(q, k_cache, v_cache, k_new, v_new, positions_dev, slots, cos_sin,
@@ -335,6 +354,21 @@ class Plan:
                                          _ptr(block_table_dev), _ptr(out), _ptr(lse),
                                          _stream_ptr(stream), arr)
         check(st, "mb_attn_forward")
+
+    def forward_fp8(self, q, k_codes, v_codes, k_scale, v_scale, block_table_dev, out,
+                    lse=None, stream=None, events=None):
+        """``mb_attn_forward_fp8``: attention over an fp8 (e4m3) cache; the plan
+        must hold no prefill items (plan with ``prefill_min_rows=-1``)."""
+        L = lib()
+        args = (self._h, _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale), _ptr(v_scale),
+                _ptr(block_table_dev), _ptr(out), _ptr(lse), _stream_ptr(stream))
+        if events is None:
+            st = L.mb_attn_forward_fp8(*args)
+        else:
+            arr = (ctypes.c_void_p * (2 * NUM_STAGES))(
+                *[None if e is None else ctypes.c_void_p(e.cuda_event) for e in events])
+            st = L.mb_attn_forward_fp8_timed(*args, arr)
+        check(st, "mb_attn_forward_fp8")
 
     def device_status(self) -> int:
         """Device error flags of this plan's workspace (synchronises)."""

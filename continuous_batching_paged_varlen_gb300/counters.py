@@ -64,11 +64,17 @@ def naive_kv_positions(requests) -> int:
 
 
 def attention_bytes(requests, block_table, n_q_heads: int, n_kv_heads: int,
-                    head_dim: int, page_size: int, elem_bytes: int = 2) -> int:
+                    head_dim: int, page_size: int, elem_bytes: int = 2,
+                    kv_elem_bytes: int | None = None, kv_row_scale_bytes: int = 0) -> int:
+    """kv_elem_bytes: bytes per cached K/V value (default elem_bytes; 1 for
+    the fp8 cache); kv_row_scale_bytes: per (position, KV head) scale bytes of
+    K and of V (4 for the fp8 cache's fp32 scales)."""
     reqs = np.asarray(requests)
     total_q = int((reqs[:, 1] - reqs[:, 0]).sum())
     qo = 2 * total_q * n_q_heads * head_dim * elem_bytes
-    kv = distinct_kv_positions(reqs, block_table, page_size) * 2 * n_kv_heads * head_dim * elem_bytes
+    kvb = elem_bytes if kv_elem_bytes is None else kv_elem_bytes
+    kv = (distinct_kv_positions(reqs, block_table, page_size) * 2 * n_kv_heads
+          * (head_dim * kvb + kv_row_scale_bytes))
     bt = int(sum((kv_len + page_size - 1) // page_size for _, _, kv_len in reqs.tolist())) * 4
     return qo + kv + bt
 
@@ -87,3 +93,9 @@ def rope_append_bytes(n_new_tokens: int, n_q_heads: int, n_kv_heads: int, head_d
     per_token = (2 * n_q_heads * head_dim * elem_bytes + 4 * n_kv_heads * head_dim * elem_bytes
                  + head_dim * 4 + 8)
     return n_new_tokens * per_token
+
+
+def append_fp8_bytes(n_new_tokens: int, n_kv_heads: int, head_dim: int) -> int:
+    """Quantizing append: read the new bf16 K and V rows, write their e4m3
+    codes and one fp32 scale per (token, KV head) row of each, + slots."""
+    return n_new_tokens * (2 * n_kv_heads * (head_dim * 2 + head_dim + 4) + 4)

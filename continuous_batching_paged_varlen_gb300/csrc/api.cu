@@ -71,6 +71,94 @@ mb_status_t mb_kv_append(void* k_cache, void* v_cache, const void* k_new, const 
   return e == cudaSuccess ? MB_OK : MB_ERR_CUDA;
 }
 
+mb_status_t mb_kv_append_fp8(void* k_codes, void* v_codes, float* k_scale, float* v_scale,
+                             const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                             int32_t T, const mb_config_t* cfg, int32_t* status_dev,
+                             cudaStream_t stream) {
+  mb_status_t st = validate_config(cfg);
+  if (st != MB_OK) return st;
+  if (T < 0) return MB_ERR_INVALID_ARG;
+  if (T == 0) return MB_OK;
+  if (!k_codes || !v_codes || !k_scale || !v_scale || !k_new || !v_new || !slot_mapping)
+    return MB_ERR_INVALID_ARG;
+  if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scale) || !aligned16(v_scale) ||
+      !aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 3) ||
+      (reinterpret_cast<uintptr_t>(status_dev) & 3))
+    return MB_ERR_INVALID_ARG;
+  cudaError_t e = launch_kv_append_fp8(k_codes, v_codes, k_scale, v_scale, k_new, v_new,
+                                       slot_mapping, T, cfg->n_kv_heads, cfg->head_dim,
+                                       cfg->page_size, cfg->num_pages, status_dev, stream);
+  return e == cudaSuccess ? MB_OK : MB_ERR_CUDA;
+}
+
+mb_status_t mb_attn_forward_fp8_timed(const mb_plan_t* plan, const void* q,
+                                      const void* k_codes, const void* v_codes,
+                                      const float* k_scale, const float* v_scale,
+                                      const int32_t* block_table_dev, void* out, float* lse,
+                                      cudaStream_t stream, cudaEvent_t* events) {
+  if (!plan || !plan->workspace) return MB_ERR_INVALID_ARG;
+  const PlanDevice& d = plan->dev;
+  if (d.n_prefill_items > 0) return MB_ERR_UNSUPPORTED;
+  if (d.total_q == 0) return MB_OK;
+  if (!q || !k_codes || !v_codes || !k_scale || !v_scale || !block_table_dev || !out)
+    return MB_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scale) ||
+      !aligned16(v_scale) || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3) ||
+      (reinterpret_cast<uintptr_t>(block_table_dev) & 3))
+    return MB_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(plan->workspace);
+  auto rec = [&](int stage, int which) {
+    if (events && events[2 * stage + which]) cudaEventRecord(events[2 * stage + which], stream);
+  };
+  cudaError_t e = cudaSuccess;
+  if (d.n_decode_items > 0) {
+    DecodeFp8Args a;
+    a.items = reinterpret_cast<const DecodeItem*>(ws + d.off_decode_items);
+    a.rows = reinterpret_cast<const RowDesc*>(ws + d.off_rows);
+    a.n_items = d.n_decode_items;
+    a.q = q;
+    a.k8 = k_codes;
+    a.v8 = v_codes;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.block_table = block_table_dev;
+    a.max_blocks = d.max_blocks;
+    a.n_q_heads = d.n_q_heads;
+    a.n_kv_heads = d.n_kv_heads;
+    a.head_dim = d.head_dim;
+    a.page_size = d.page_size;
+    a.num_pages = d.num_pages;
+    a.scale_log2 = d.scale * kLog2e;
+    a.out = out;
+    a.lse = lse;
+    a.part_o = reinterpret_cast<float*>(ws + d.off_part_o);
+    a.part_lse = reinterpret_cast<float*>(ws + d.off_part_lse);
+    a.status = reinterpret_cast<int32_t*>(ws);
+    rec(MB_STAGE_DECODE, 0);
+    e = launch_decode_fp8(a, stream);
+    rec(MB_STAGE_DECODE, 1);
+    if (e != cudaSuccess) return MB_ERR_CUDA;
+  }
+  if (d.n_combine > 0) {
+    rec(MB_STAGE_COMBINE, 0);
+    e = launch_combine(reinterpret_cast<const CombineEntry*>(ws + d.off_combine), d.n_combine,
+                       reinterpret_cast<const float*>(ws + d.off_part_o),
+                       reinterpret_cast<const float*>(ws + d.off_part_lse), d.head_dim,
+                       d.n_q_heads, out, lse, stream, events == nullptr);
+    rec(MB_STAGE_COMBINE, 1);
+    if (e != cudaSuccess) return MB_ERR_CUDA;
+  }
+  return MB_OK;
+}
+
+mb_status_t mb_attn_forward_fp8(const mb_plan_t* plan, const void* q, const void* k_codes,
+                                const void* v_codes, const float* k_scale, const float* v_scale,
+                                const int32_t* block_table_dev, void* out, float* lse,
+                                cudaStream_t stream) {
+  return mb_attn_forward_fp8_timed(plan, q, k_codes, v_codes, k_scale, v_scale,
+                                   block_table_dev, out, lse, stream, nullptr);
+}
+
 mb_status_t mb_rope_table(float* cos_sin, int32_t max_position, int32_t head_dim, float base) {
   if (!cos_sin || max_position <= 0 || head_dim <= 0 || (head_dim & 1) || !(base > 0.0f) ||
       !isfinite(base))

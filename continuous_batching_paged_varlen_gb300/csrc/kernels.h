@@ -15,6 +15,12 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new,
                              int32_t n_kv_heads, int32_t head_dim, int32_t page_size,
                              int32_t num_pages, int32_t* status, cudaStream_t s);
 
+// KV append into an fp8 (e4m3) cache with per-row fp32 scales (kv_append.cu).
+cudaError_t launch_kv_append_fp8(void* k8, void* v8, float* ks, float* vs, const void* k_new,
+                                 const void* v_new, const int32_t* slots, int32_t T,
+                                 int32_t n_kv_heads, int32_t head_dim, int32_t page_size,
+                                 int32_t num_pages, int32_t* status, cudaStream_t s);
+
 // Fused rotary embedding + KV append (rope_append.cu).
 cudaError_t launch_rope_append(void* q, void* k_cache, void* v_cache, const void* k_new,
                                const void* v_new, const int32_t* positions,
@@ -46,6 +52,28 @@ struct DecodeArgs {
 // kernel may start while the previous kernel on the stream (which must not
 // produce anything it reads) is still running.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, bool overlap_previous = false);
+
+// Split-KV / cascade kernel over an fp8 (e4m3) cache with per-row fp32
+// scales (decode_fp8.cu). Same work lists and outputs as launch_decode.
+struct DecodeFp8Args {
+  const DecodeItem* items;
+  const RowDesc* rows;
+  int32_t n_items;
+  const void* q;
+  const void* k8;         // e4m3 codes [pages, Hkv, ps, D]
+  const void* v8;
+  const float* k_scale;   // [pages, Hkv, ps]
+  const float* v_scale;
+  const int32_t* block_table;
+  int32_t max_blocks, n_q_heads, n_kv_heads, head_dim, page_size, num_pages;
+  float scale_log2;
+  void* out;
+  float* lse;
+  float* part_o;
+  float* part_lse;
+  int32_t* status;
+};
+cudaError_t launch_decode_fp8(const DecodeFp8Args& a, cudaStream_t s);
 
 // LSE merge of partials (combine.cu). overlap_previous: launch with
 // programmatic stream serialization after the split-KV kernel (the combine

@@ -84,3 +84,90 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new,
 }
 
 }  // namespace mb
+
+// ---------------------------------------------------------------------------
+// fp8 (e4m3) cache: quantize while appending.
+//
+// "GLM-5.3 e2e token ledger", the KV layout paragraphs: FP8 K/V with FP32
+// scales kept next to the data (one per 128 values), read together by the
+// attention kernel to dequantize. Here: one fp32 scale per (token, KV head)
+// row, scale = amax(|row|) / 448, code = e4m3(x / scale) rounded to nearest
+// (ties to even), saturating; a zero row gets scale 0 and zero codes. The
+// quotient is one IEEE fp32 division, so the codes are reproducible.
+// One warp per row: each lane holds D/32 consecutive values.
+namespace mb {
+namespace {
+
+template <int D>
+__global__ void __launch_bounds__(128) kv_append_fp8_kernel(
+    uint8_t* __restrict__ k8, uint8_t* __restrict__ v8, float* __restrict__ ks,
+    float* __restrict__ vs, const __nv_bfloat16* __restrict__ kn,
+    const __nv_bfloat16* __restrict__ vn, const int32_t* __restrict__ slots, int32_t Hkv,
+    int32_t ps_shift, int64_t n_slots, int32_t* status) {
+  constexpr int E = D / 32;  // values per lane (4 for D = 128, 2 for D = 64)
+  const int t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int32_t slot = __ldg(slots + t);
+  if (slot < 0) return;
+  if ((int64_t)slot >= n_slots) {
+    if (threadIdx.x == 0) dev::set_status(status, MB_ERR_DEVICE_INDEX);
+    return;
+  }
+  const int32_t page = slot >> ps_shift;
+  const int32_t off = slot & ((1 << ps_shift) - 1);
+  for (int row = warp; row < 2 * Hkv; row += 4) {
+    const int h = row < Hkv ? row : row - Hkv;
+    const __nv_bfloat16* src = (row < Hkv ? kn : vn) + ((int64_t)t * Hkv + h) * D + E * lane;
+    float x[E];
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      x[e] = __bfloat162float(src[e]);
+      amax = fmaxf(amax, fabsf(x[e]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = __fdiv_rn(amax, 448.0f);
+    uint8_t code[E];
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      uint16_t pair = 0;
+      if (scale > 0.f) {
+        const float a = __fdiv_rn(x[e], scale), b = __fdiv_rn(x[e + 1], scale);
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(b), "f"(a));
+      }
+      code[e] = (uint8_t)(pair & 0xff);
+      code[e + 1] = (uint8_t)(pair >> 8);
+    }
+    const int64_t drow = (((int64_t)page * Hkv + h) << ps_shift) + off;
+    uint8_t* dst = (row < Hkv ? k8 : v8) + drow * D + E * lane;
+    if constexpr (E == 4) {
+      *reinterpret_cast<uint32_t*>(dst) = (uint32_t)code[0] | ((uint32_t)code[1] << 8) |
+                                          ((uint32_t)code[2] << 16) | ((uint32_t)code[3] << 24);
+    } else {
+      *reinterpret_cast<uint16_t*>(dst) = (uint16_t)(code[0] | (code[1] << 8));
+    }
+    if (lane == 0) (row < Hkv ? ks : vs)[drow] = scale;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append_fp8(void* k8, void* v8, float* ks, float* vs, const void* k_new,
+                                 const void* v_new, const int32_t* slots, int32_t T,
+                                 int32_t n_kv_heads, int32_t head_dim, int32_t page_size,
+                                 int32_t num_pages, int32_t* status, cudaStream_t s) {
+  const int ps_shift = __builtin_ctz((unsigned)page_size);
+  const int64_t n_slots = (int64_t)num_pages * page_size;
+  if (head_dim == 128)
+    kv_append_fp8_kernel<128><<<(unsigned)T, 128, 0, s>>>(
+        (uint8_t*)k8, (uint8_t*)v8, ks, vs, (const __nv_bfloat16*)k_new,
+        (const __nv_bfloat16*)v_new, slots, n_kv_heads, ps_shift, n_slots, status);
+  else
+    kv_append_fp8_kernel<64><<<(unsigned)T, 128, 0, s>>>(
+        (uint8_t*)k8, (uint8_t*)v8, ks, vs, (const __nv_bfloat16*)k_new,
+        (const __nv_bfloat16*)v_new, slots, n_kv_heads, ps_shift, n_slots, status);
+  return cudaGetLastError();
+}
+
+}  // namespace mb

@@ -170,6 +170,54 @@ mb_status_t mb_kv_append(void* k_cache, void* v_cache, const void* k_new,
                          int32_t T, const mb_config_t* cfg, int32_t* status_dev,
                          cudaStream_t stream);
 
+/* fp8 (e4m3) KV cache ("GLM-5.3 e2e token ledger", the KV layout
+ * paragraphs: FP8 K/V with FP32 scales stored beside them, read together by
+ * the attention kernel to dequantize). Layout, all device memory:
+ *   k_codes, v_codes  [num_pages, n_kv_heads, page_size, head_dim] uint8
+ *                     e4m3 codes (1 sign, 4 exponent bits with bias 7,
+ *                     3 mantissa bits, no infinities; 0x7F/0xFF are NaN)
+ *   k_scale, v_scale  [num_pages, n_kv_heads, page_size] fp32, one scale
+ *                     per (token, KV head) row
+ * and a row's values are decode(code) * scale.
+ *
+ * Append with quantization: for every token t with slot = slot_mapping[t]
+ * >= 0 and every KV head h, the bf16 row x = k_new[t][h] (and likewise
+ * v_new) is stored as scale = amax(|x|) / 448 (fp32 division; 448 = the
+ * largest e4m3 value) and code_i = e4m3(x_i / scale) (one IEEE fp32
+ * division, round to nearest even, saturating at +-448, the sign kept for
+ * values that round to zero); an all-zero row gets scale 0 and codes 0.
+ * Slot rules, status bits, alignment (every pointer 16-byte aligned) and
+ * errors as for mb_kv_append. */
+mb_status_t mb_kv_append_fp8(void* k_codes, void* v_codes, float* k_scale, float* v_scale,
+                             const void* k_new, const void* v_new,
+                             const int32_t* slot_mapping, int32_t T,
+                             const mb_config_t* cfg, int32_t* status_dev,
+                             cudaStream_t stream);
+
+/* Attention of every planned request over an fp8 cache (layout above):
+ * the same result as mb_attn_forward on the dequantized K/V. Only the
+ * split-KV path reads fp8 pages: the plan must hold no prefill items (build
+ * it with mb_plan_options_t.prefill_min_rows = -1), else
+ * MB_ERR_UNSUPPORTED and nothing is enqueued. Q K^T runs on f16 operands
+ * (q is rounded once from bf16 to f16, saturating at +-65504; every e4m3
+ * code is exact in f16) and P V on bf16 operands, fp32 accumulation. Other
+ * arguments, outputs and errors as for mb_attn_forward; all pointers 16-byte
+ * aligned (lse 4). */
+mb_status_t mb_attn_forward_fp8(const mb_plan_t* plan, const void* q,
+                                const void* k_codes, const void* v_codes,
+                                const float* k_scale, const float* v_scale,
+                                const int32_t* block_table_dev, void* out,
+                                float* lse, cudaStream_t stream);
+
+/* mb_attn_forward_fp8 with per-stage events (MB_STAGE_DECODE, MB_STAGE_COMBINE),
+ * as mb_attn_forward_timed. */
+mb_status_t mb_attn_forward_fp8_timed(const mb_plan_t* plan, const void* q,
+                                      const void* k_codes, const void* v_codes,
+                                      const float* k_scale, const float* v_scale,
+                                      const int32_t* block_table_dev, void* out,
+                                      float* lse, cudaStream_t stream,
+                                      cudaEvent_t* events);
+
 /* Rotary angle table for mb_rope_kv_append (host helper, no CUDA call).
  * cos_sin (host, max_position * head_dim floats) row p receives
  * [cos(p theta_0) .. cos(p theta_{D/2-1}), sin(p theta_0) .. sin(p theta_{D/2-1})],
