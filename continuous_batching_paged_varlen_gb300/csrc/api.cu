@@ -33,16 +33,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 128-byte-swizzled bf16 tensor map; dims/strides innermost first, strides
-// for dims 1.. in bytes.
+// Tiled tensor map; dims/strides innermost first, strides for dims 1.. in
+// bytes. Default: 128-byte-swizzled bf16.
 bool make_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-              const cuuint64_t* strides, const cuuint32_t* box) {
+              const cuuint64_t* strides, const cuuint32_t* box,
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return false;
   cuuint32_t elem[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
-                  dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  CUresult r = fn(map, dtype, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, elem,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -112,7 +113,18 @@ mb_status_t mb_attn_forward_fp8_timed(const mb_plan_t* plan, const void* q,
   };
   cudaError_t e = cudaSuccess;
   if (d.n_decode_items > 0) {
+    // K codes as rows of head_dim bytes, one page of one KV head per box,
+    // swizzled into the K-major operand layout of the e4m3 MMA
+    CUtensorMap km;
+    const cuuint64_t kdims[2] = {(cuuint64_t)d.head_dim,
+                                 (cuuint64_t)d.num_pages * d.n_kv_heads * d.page_size};
+    const cuuint64_t kstr[1] = {(cuuint64_t)d.head_dim};
+    const cuuint32_t kbox[2] = {(cuuint32_t)d.head_dim, (cuuint32_t)d.page_size};
+    if (!make_map(&km, k_codes, 2, kdims, kstr, kbox, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                  d.head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+      return MB_ERR_CUDA;
     DecodeFp8Args a;
+    a.k_map = &km;
     a.items = reinterpret_cast<const DecodeItem*>(ws + d.off_decode_items);
     a.rows = reinterpret_cast<const RowDesc*>(ws + d.off_rows);
     a.n_items = d.n_decode_items;

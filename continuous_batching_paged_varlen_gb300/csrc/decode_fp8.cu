@@ -9,30 +9,42 @@
 // Scale Your Model notes (7-8)", section 3), and the results are the same
 // final rows or normalised partials for the combine kernel.
 //
-// The scale of key j factors out of both products:
-//   S[r][j] = ks_j * (q_r . kcode_j)       O[r] = sum_j (p[r][j] * vs_j) vcode_j
-// so the tensor core multiplies raw codes and the softmax applies ks_j to
-// the scores and folds vs_j into P. Every e4m3 value is exact in f16 and in
-// bf16, so the operands lose nothing: Q K^T runs on f16 operands (Q is
-// rounded from bf16 to f16 once, saturating at +-65504) and P V on bf16
-// operands, both with fp32 accumulation in TMEM.
+// The scales of key j factor out of both products:
+//   S[r][j] = ks_j sq_r (qc_r . kcode_j)    O[r] = rho sum_j (p[r][j] vs_j / rho) vcode_j
+//   * Q K^T runs on the raw e4m3 K codes (kind::f8f6f4, fp32 accumulation):
+//     each query row q is written as sq (hi + lo) with sq = amax|q| / 448,
+//     hi = e4m3(q / sq) and lo = e4m3(q / sq - hi), two e4m3 rows whose
+//     products with the K tile add up in the same accumulator. hi + lo holds
+//     q to about 2^-8 of each value (near bf16's 2^-9), so the split costs
+//     the scores about what bf16 Q costs them, and no K value is converted.
+//   * P' V runs on f16 operands (every e4m3 value is exact in f16), with
+//     P' = p vs_j / rho. rho is a power of two at least as large as every V
+//     scale seen so far; it only grows, and O is rescaled by the exact ratio
+//     when it does, so P' stays within [0, 2^8] whatever the magnitude of V.
+//   The softmax applies ks_j sq_r (times log2(e) and the softmax scale) to
+//   the scores.
 //
-// Half the bytes of the bf16 cache per key, so the pipeline adds a stage
-// that turns the staged codes into MMA operands:
-//   warp 8      producer: for each 128-key tile, one bulk copy per page of
-//               codes (a page of one KV head is ps * D contiguous bytes) and
-//               one of its ps scales, K then V, into a staging ring.
-//   warps 4-7   converters: staged codes -> 16-bit operand tiles in the
-//               128-byte-swizzled K-major layout (K as f16, V as bf16, V rows
-//               past k_end zeroed), and the tile's scales (ks * log2(e) *
-//               softmax scale, vs) into a small ring the softmax reads.
-//   warp 9      TMEM allocation; one lane issues S = Q K^T and O += P V.
-//   warps 0-3   softmax. With few rows (a decode step's g query heads), each
-//               row is copied into 4 (or 2) TMEM lanes of different warps and
-//               each copy handles 32 (or 64) of the tile's 128 keys, so the
-//               exponentials of one row spread over 4 SM sub-partitions; the
-//               copies agree on the running max through shared memory every
-//               tile and add their partial sums and outputs at the end.
+// Roles (320 threads):
+//   warp 8      producer, in the order the tensor core consumes the tiles
+//               (K0 K1 V0 K2 V1 K3 V2 ...): K tiles by TMA, one box per page,
+//               straight into the 128-byte (64-byte for D = 64) swizzled
+//               K-major operand layout of a 6-slot ring (8 for D = 64); V
+//               codes by bulk copy into a staging ring; each page's ps scales
+//               by bulk copy beside them.
+//   warps 4-7   V converters: 16 staged codes -> 8 f16x2 words per task into
+//               the operand tiles of a 2-slot ring (rows past k_end zeroed);
+//               the V scales and their largest value go to a small ring the
+//               softmax reads.
+//   warp 9      TMEM allocation; one lane issues S = Q K^T (the hi and lo
+//               rows of Q from TMEM) and O += P' V (P' from TMEM).
+//   warps 0-3   softmax; each thread first writes its query row's hi / lo
+//               codes to TMEM. With few rows (a decode step's g query heads),
+//               each row is copied into 4 (or 2) TMEM lanes of different
+//               warps and each copy handles 32 (or 64) of the tile's 128
+//               keys, so the exponentials of one row spread over the 4 SM
+//               sub-partitions; the copies agree on the running max through
+//               shared memory every tile and add their partial sums and
+//               outputs at the end.
 // Every wait is bounded; on a timeout the CTA raises its abort flag, drains
 // what it issued, frees its TMEM and returns.
 #include <cuda_runtime.h>
@@ -51,28 +63,32 @@ constexpr int BM = 128;  // TMEM lanes (query rows, possibly copied)
 constexpr int BN = 128;  // keys per tile
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;  // + 128 * buffer
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColS = 0;    // + 128 * buffer
+constexpr uint32_t kColO = 256;  // D columns
+constexpr uint32_t kColQ = 384;  // hi codes (D / 4 columns), then lo codes
 constexpr float kRescaleThreshold = 8.0f;
 constexpr uint64_t kDrainNs = 200000000ull;
-constexpr int kOpSlots = 3;   // 16-bit operand tiles: K_j, V_j, K_j+1, ...
-constexpr int kScSlots = 4;   // per-tile scale vectors
-constexpr int kMaxStSlots = 8;
+constexpr int kVOpSlots = 2;          // f16 V operand tiles
+constexpr int kScSlots = 4;           // per-tile V scale vectors
+constexpr int kScFloats = BN + 4;     // vs [BN], max vs per converter warp
+constexpr int kMaxSlots = 8;
 
 enum {
-  B_ST_FULL = 0,                           // + staging slot
-  B_ST_EMPTY = B_ST_FULL + kMaxStSlots,    // + staging slot
-  B_OP_FULL = B_ST_EMPTY + kMaxStSlots,    // + operand slot
-  B_OP_EMPTY = B_OP_FULL + kOpSlots,       // + operand slot
-  B_SCK_FULL = B_OP_EMPTY + kOpSlots,      // + scale slot
-  B_SCV_FULL = B_SCK_FULL + kScSlots,      // + scale slot
-  B_SC_EMPTY = B_SCV_FULL + kScSlots,      // + scale slot
-  B_S_FULL = B_SC_EMPTY + kScSlots,        // + S buffer
+  B_K_FULL = 0,                          // + K slot
+  B_K_EMPTY = B_K_FULL + kMaxSlots,      // + K slot (MMA commit + 4 softmax warps)
+  B_VS_FULL = B_K_EMPTY + kMaxSlots,     // + V staging slot
+  B_VS_EMPTY = B_VS_FULL + kMaxSlots,    // + V staging slot
+  B_VO_FULL = B_VS_EMPTY + kMaxSlots,    // + V operand slot
+  B_VO_EMPTY = B_VO_FULL + kVOpSlots,    // + V operand slot
+  B_SCV_FULL = B_VO_EMPTY + kVOpSlots,   // + scale slot
+  B_SC_EMPTY = B_SCV_FULL + kScSlots,    // + scale slot
+  B_S_FULL = B_SC_EMPTY + kScSlots,      // + S buffer
   B_P_FULL = B_S_FULL + 2,
   B_O_DONE = B_P_FULL + 1,
-  B_RED_FULL = B_O_DONE + 1,               // + buffer
+  B_RED_FULL = B_O_DONE + 1,             // + buffer
   B_EPI_FULL = B_RED_FULL + 2,
-  B_MMA_DONE = B_EPI_FULL + 1,
+  B_Q_READY = B_EPI_FULL + 1,
+  B_MMA_DONE = B_Q_READY + 1,
   B_COUNT = B_MMA_DONE + 1
 };
 
@@ -80,30 +96,46 @@ template <int D>
 struct Layout {
   static constexpr int kHalves = D / 64;
   static constexpr uint32_t kHalfBytes = 128 * 128;  // 128 rows x 64 16-bit values
-  static constexpr uint32_t kTileBytes = kHalves * kHalfBytes;
-  static constexpr int kStSlots = D == 128 ? 4 : 8;
-  static constexpr uint32_t kStCodes = BN * D;             // codes of one staged tile
-  static constexpr uint32_t kStBytes = kStCodes + BN * 4;  // + its scales
-  static constexpr uint32_t q_off = 0;
-  static constexpr uint32_t op_off = kTileBytes;
-  static constexpr uint32_t st_off = op_off + kOpSlots * kTileBytes;
-  static constexpr uint32_t sc_off = st_off + kStSlots * kStBytes;
-  static constexpr uint32_t redm_off = sc_off + kScSlots * 2 * BN * 4;  // float [2][4][32]
-  static constexpr uint32_t redl_off = redm_off + 2 * 4 * 32 * 4;       // float [4][32]
+  static constexpr uint32_t kVOpBytes = kHalves * kHalfBytes;
+  static constexpr uint32_t kCodes = BN * D;  // e4m3 codes of one tile
+  // K slot: the swizzled code tile, then its scales, padded to 1024 bytes
+  static constexpr uint32_t kKSlot = (kCodes + BN * 4 + 1023) & ~1023u;
+  static constexpr int kKSlots = D == 128 ? 6 : 8;
+  static constexpr uint32_t kVStBytes = kCodes + BN * 4;
+  static constexpr int kVStSlots = D == 128 ? 3 : 6;
+  static constexpr uint32_t k_off = 0;
+  static constexpr uint32_t vop_off = k_off + kKSlots * kKSlot;
+  static constexpr uint32_t vst_off = vop_off + kVOpSlots * kVOpBytes;
+  static constexpr uint32_t sc_off = vst_off + kVStSlots * kVStBytes;
+  static constexpr uint32_t redm_off = sc_off + kScSlots * kScFloats * 4;  // float [2][4][32]
+  static constexpr uint32_t redl_off = redm_off + 2 * 4 * 32 * 4;           // float [4][32]
   static constexpr uint32_t bar_off = redl_off + 4 * 32 * 4;
   static constexpr uint32_t misc_off = bar_off + B_COUNT * 8;
   static constexpr uint32_t kBytes = misc_off + 16;
   // more than half the SM so that one CTA holds the SM's 512 TMEM columns
   static constexpr uint32_t kAlloc =
       (kBytes + 1024 > 232448u / 2 + 1024) ? kBytes + 1024 : 232448u / 2 + 1024;
-  // the epilogue adds the row copies' outputs in the (then idle) operand ring
+  // the epilogue adds the row copies' outputs in the (then idle) K ring
   static constexpr int kRedRow = D + 4;  // floats per row, padded against bank conflicts
-  static_assert(kStSlots <= kMaxStSlots, "staging ring");
-  static_assert(4 * 32 * kRedRow * 4 <= kOpSlots * kTileBytes, "reduction buffer");
+  static_assert(kKSlots <= kMaxSlots && kVStSlots <= kMaxSlots, "rings");
+  static_assert(4 * 32 * kRedRow * 4 <= kKSlots * kKSlot, "reduction buffer");
   static_assert(kAlloc <= 232448, "shared memory");
 };
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Position s of the tile stream K0 K1 V0 K2 V1 ... K(n-1) V(n-2) V(n-1)
+// (the order the MMA lane consumes them: S(j+1) is issued before P V(j)).
+struct SeqItem {
+  int j;
+  bool v;
+};
+__device__ __forceinline__ SeqItem seq_item(int s, int n) {
+  if (s == 0) return {0, false};
+  const int m = s >> 1;
+  if (s & 1) return (m + 1 < n) ? SeqItem{m + 1, false} : SeqItem{m, true};
+  return {m - 1, true};
+}
 
 // Two e4m3 codes (low byte first) -> f16x2 (exact).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
@@ -111,28 +143,78 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((unsigned short)(two & 0xffffu)));
   return r;
 }
-// f16x2 -> bf16x2, exact for values that fit both formats (every e4m3 value).
-__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
-  float lo, hi;
+// (lo, hi) fp32 -> two e4m3 codes (lo in the low byte), nearest, saturating.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ void f16x2_to_f32x2(uint32_t h, float& lo, float& hi) {
   asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
       : "=f"(lo), "=f"(hi)
       : "r"(h));
-  return pack_bf16x2(lo, hi);
 }
-// bf16x2 -> f16x2, round to nearest, saturating at +-65504.
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u) {
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
-  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(bf16_hi(u)), "f"(bf16_lo(u)));
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+// Smallest power of two >= x, for finite x > 0.
+__device__ __forceinline__ float pow2_ceil(float x) {
+  const uint32_t b = __float_as_uint(x);
+  uint32_t e = b & 0x7f800000u;
+  if ((b & 0x007fffffu) != 0u || e == 0u) e += 0x00800000u;
+  return __uint_as_float(e);
+}
+// Four scaled values y0..y3 -> hi codes and lo codes (lo = e4m3(y - hi)),
+// one 32-bit word each, y0 in the lowest byte.
+__device__ __forceinline__ void split4(float y0, float y1, float y2, float y3, uint32_t& hi,
+                                       uint32_t& lo) {
+  const uint32_t h01 = f32x2_to_e4m3x2(y0, y1), h23 = f32x2_to_e4m3x2(y2, y3);
+  float d0, d1, d2, d3;
+  f16x2_to_f32x2(e4m3x2_to_f16x2(h01), d0, d1);
+  f16x2_to_f32x2(e4m3x2_to_f16x2(h23), d2, d3);
+  hi = h01 | (h23 << 16);
+  lo = f32x2_to_e4m3x2(y0 - d0, y1 - d1) | (f32x2_to_e4m3x2(y2 - d2, y3 - d3) << 16);
+}
+
+// Shared-memory loads by shared-window address. The softmax reaches its
+// buffers through a struct of pointers, where the compiler cannot see the
+// state space and would issue generic loads; these stay ld.shared. They are
+// volatile so that none moves above the barrier wait that publishes the data.
+__device__ __forceinline__ float4 lds4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint4 lds4u(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts4u(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ float lds1(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
 }
 
 struct Shared {
   uint64_t* bars;
   volatile int* abort_flag;
-  const float* sc;  // [kScSlots][2][BN]: ks * scale_log2, vs
-  float* redm;      // [2][4][32]
-  float* redl;      // [4][32]
-  float* redo;      // [4][32][D + 4] (operand ring, epilogue only)
+  const uint8_t* kring;  // K slots (codes, then scales)
+  const float* sc;       // [kScSlots][kScFloats]
+  float* redm;           // [2][4][32]
+  float* redl;           // [4][32]
+  float* redo;           // [4][32][D + 4] (K ring, epilogue only)
   uint32_t tmem;
 };
 
@@ -155,26 +237,80 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
   rd.vis_end = 0;
   rd.dst = -1;
   if (valid) rd = a.rows[it.row_begin + r];
-  const int vis_hi = min(it.k_end, rd.vis_end);
   const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+
+  // this lane's query row as sq * (hi + lo), the hi / lo codes into TMEM
+  // (the A operands of Q K^T); lanes without a row hold zeros
+  float sq = 0.f;
+  {
+    const uint4* qrow = static_cast<const uint4*>(a.q) +
+                        ((int64_t)rd.q_index * a.n_q_heads + rd.q_head) * (D / 8);
+    float amax = 0.f;
+    if (valid) {
+#pragma unroll 4
+      for (int k = 0; k < D / 8; ++k) {
+        const uint4 b = __ldg(qrow + k);
+        const uint32_t wv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          amax = fmax3(amax, fabsf(bf16_lo(wv[e])), fabsf(bf16_hi(wv[e])));
+      }
+    }
+    sq = amax * (1.f / 448.f);
+    const float inv = amax > 0.f ? 448.f / amax : 0.f;
+    constexpr int QW = D / 4;  // 32-bit columns per code row
+    constexpr int QH = QW < 32 ? QW : 32;
+#pragma unroll
+    for (int hh = 0; hh < QW / QH; ++hh) {
+      uint32_t hi[QH], lo[QH];
+#pragma unroll
+      for (int k = 0; k < QH / 2; ++k) {  // one 16-byte chunk = 8 values = 2 columns
+        uint4 b = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) b = __ldg(qrow + hh * (QH / 2) + k);
+        split4(bf16_lo(b.x) * inv, bf16_hi(b.x) * inv, bf16_lo(b.y) * inv, bf16_hi(b.y) * inv,
+               hi[2 * k], lo[2 * k]);
+        split4(bf16_lo(b.z) * inv, bf16_hi(b.z) * inv, bf16_lo(b.w) * inv, bf16_hi(b.w) * inv,
+               hi[2 * k + 1], lo[2 * k + 1]);
+      }
+      if constexpr (QH == 32) {
+        tmem_st32(sh.tmem + lane_addr + kColQ + 32 * hh, hi);
+        tmem_st32(sh.tmem + lane_addr + kColQ + QW + 32 * hh, lo);
+      } else {
+        tmem_st16(sh.tmem + lane_addr + kColQ, hi);
+        tmem_st16(sh.tmem + lane_addr + kColQ + QW, lo);
+      }
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[B_Q_READY]);
+  }
+
+  const int vis_hi = min(it.k_end, rd.vis_end);
   const uint32_t o_col = sh.tmem + lane_addr + kColO;
   const int col0 = c * W;
+  const float crow = a.scale_log2 * sq;  // this row's factor of every score
   float m = -INFINITY, l = 0.f;
+  float rho = 0.f, inv_rho = 0.f;  // V-scale reference (power of two), its inverse
   bool ok = true;
   for (int j = 0; j < n; ++j) {
     const int sc = j % kScSlots;
     const uint32_t scph = (uint32_t)(j / kScSlots) & 1u;
+    const int ks_slot = j % L::kKSlots;
+    const float* scv = sh.sc + sc * kScFloats;
     const uint32_t p_col = sh.tmem + lane_addr + kColS + 128 * (j & 1);
     ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_S_FULL + (j & 1)], (uint32_t)(j >> 1) & 1u,
                                            sh.abort_flag, a.status));
     if (!ok) break;
     tc_fence_after();
-    ok = __all_sync(0xffffffffu,
-                    mbar_wait(&bars[B_SCK_FULL + sc], scph, sh.abort_flag, a.status));
+    // the K tile's scales arrived with its codes
+    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_K_FULL + ks_slot],
+                                           (uint32_t)(j / L::kKSlots) & 1u, sh.abort_flag,
+                                           a.status));
     if (!ok) break;
-    // scores in the log2 domain: ks_j * log2(e) * scale * (q . kcode_j),
-    // keys past the row's visibility bound at -inf
-    const float* kf = sh.sc + sc * 2 * BN + col0;
+    // scores in the log2 domain: ks_j sq log2(e) scale (qc . kcode_j), keys
+    // past the row's visibility bound at -inf
+    const uint32_t kf = smem_u32(sh.kring + ks_slot * L::kKSlot + L::kCodes) + 4 * col0;
     const int lim = vis_hi - (it.k_begin + j * BN) - col0;  // columns e < lim are visible
     // up to 64 columns stay in registers; 128 take a second pass over TMEM
     // (the max first, then the exponentials), which keeps the role within
@@ -186,12 +322,13 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
       tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(x));
 #pragma unroll
       for (int e4 = 0; e4 < 8; ++e4) {
-        const float4 f = reinterpret_cast<const float4*>(kf + 32 * h)[e4];
+        const float4 f = lds4(kf + 4 * (32 * h + 4 * e4));
         const float fv[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int e = 4 * e4 + q;
-          x[e] = __float_as_uint(32 * h + e < lim ? __uint_as_float(x[e]) * fv[q] : -INFINITY);
+          x[e] = __float_as_uint(32 * h + e < lim ? __uint_as_float(x[e]) * (fv[q] * crow)
+                                                  : -INFINITY);
         }
       }
     };
@@ -213,7 +350,8 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
                                              (uint32_t)(j >> 1) & 1u, sh.abort_flag, a.status));
       if (!ok) break;
 #pragma unroll
-      for (int cc = 0; cc < R; ++cc) mx = fmaxf(mx, red[(g + ngrp * cc) * 32 + lane]);
+      for (int cc = 0; cc < R; ++cc)
+        mx = fmaxf(mx, lds1(smem_u32(red + (g + ngrp * cc) * 32 + lane)));
     }
     const float m_new = fmaxf(m, mx);
     float alpha = 1.f;
@@ -230,10 +368,25 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
     ok = __all_sync(0xffffffffu,
                     mbar_wait(&bars[B_SCV_FULL + sc], scph, sh.abort_flag, a.status));
     if (!ok) break;
-    // P' = p * vs_j in bf16, stored 16 packed columns (32 keys) at a time
-    // into S buffer j & 1 (P(j-1) V(j-1) reads the other one); the other
-    // copies' columns are zero
-    const float4* vf = reinterpret_cast<const float4*>(sh.sc + sc * 2 * BN + BN + col0);
+    // the V-scale reference grows (by an exact power of two) to cover this
+    // tile's largest scale; the same for every thread of the CTA
+    {
+      const float4 v4 = lds4(smem_u32(scv + BN));
+      const float vmx = fmaxf(fmaxf(v4.x, v4.y), fmaxf(v4.z, v4.w));
+      if (vmx > rho) {
+        const float nr = pow2_ceil(vmx);
+        if (rho > 0.f) {
+          alpha *= rho / nr;
+          need = true;
+        }
+        rho = nr;
+        inv_rho = 1.f / nr;
+      }
+    }
+    // P' = p * vs_j / rho in f16, stored 16 packed columns (32 keys) at a
+    // time into S buffer j & 1 (P(j-1) V(j-1) reads the other one); the
+    // other copies' columns are zero
+    const uint32_t vf = smem_u32(scv + col0);
     float sum[2] = {0.f, 0.f};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -246,15 +399,15 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
         if (W > 64) scaled_chunk(h, x);
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 f = vf[8 * h + e4];
+          const float4 f = lds4(vf + 16 * (8 * h + e4));
           const float p0 = fast_exp2(__uint_as_float(x[4 * e4]) - mc);
           const float p1 = fast_exp2(__uint_as_float(x[4 * e4 + 1]) - mc);
           const float p2 = fast_exp2(__uint_as_float(x[4 * e4 + 2]) - mc);
           const float p3 = fast_exp2(__uint_as_float(x[4 * e4 + 3]) - mc);
           sum[0] += p0 + p2;
           sum[1] += p1 + p3;
-          pk[2 * e4] = pack_bf16x2(p0 * f.x, p1 * f.y);
-          pk[2 * e4 + 1] = pack_bf16x2(p2 * f.z, p3 * f.w);
+          pk[2 * e4] = pack_f16x2(p0 * (f.x * inv_rho), p1 * (f.y * inv_rho));
+          pk[2 * e4 + 1] = pack_f16x2(p2 * (f.z * inv_rho), p3 * (f.w * inv_rho));
         }
       } else {
 #pragma unroll
@@ -264,7 +417,10 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
     }
     l += sum[0] + sum[1];
     __syncwarp();
-    if (lane == 0) mbar_arrive(&bars[B_SC_EMPTY + sc]);
+    if (lane == 0) {
+      mbar_arrive(&bars[B_SC_EMPTY + sc]);
+      mbar_arrive(&bars[B_K_EMPTY + ks_slot]);  // done with the K tile's scales
+    }
     // O may be rescaled once P(j-1) V(j-1) completed; waiting every tile
     // also keeps this barrier's phases in step
     if (j > 0) {
@@ -273,7 +429,7 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
       if (!ok) break;
     }
     tc_fence_after();
-    if (__any_sync(0xffffffffu, need)) {
+    if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -298,7 +454,7 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
   const int64_t orow = (int64_t)rd.q_index * a.n_q_heads + rd.q_head;
   if constexpr (R == 1) {
     const bool any = l > 0.f;
-    const float inv = any ? 1.f / l : 0.f;
+    const float inv = any ? rho / l : 0.f;
     const float lse2 = any ? m + log2f(l) : -INFINITY;
     uint4* dst_out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * D);
     float4* dst_part = reinterpret_cast<float4*>(a.part_o + (int64_t)max(rd.dst, 0) * D);
@@ -351,9 +507,9 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
       return;
     float lt = 0.f;
 #pragma unroll
-    for (int cc = 0; cc < R; ++cc) lt += sh.redl[(g + ngrp * cc) * 32 + lane];
+    for (int cc = 0; cc < R; ++cc) lt += lds1(smem_u32(sh.redl + (g + ngrp * cc) * 32 + lane));
     const bool any = lt > 0.f;
-    const float inv = any ? 1.f / lt : 0.f;
+    const float inv = any ? rho / lt : 0.f;
     const float lse2 = any ? m + log2f(lt) : -INFINITY;
     constexpr int CW = D / R;  // columns this warp finishes
     const int cbeg = c * CW;
@@ -364,8 +520,7 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int cc = 0; cc < R; ++cc) {
-          const float4 v = *reinterpret_cast<const float4*>(
-              sh.redo + ((g + ngrp * cc) * 32 + lane) * RR + col);
+          const float4 v = lds4(smem_u32(sh.redo + ((g + ngrp * cc) * 32 + lane) * RR + col));
           acc.x += v.x;
           acc.y += v.y;
           acc.z += v.z;
@@ -391,14 +546,15 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    splitkv_fp8_kernel(const DecodeFp8Args a, const int ps_shift) {
+    splitkv_fp8_kernel(const DecodeFp8Args a, const int ps_shift,
+                       const __grid_constant__ CUtensorMap k_map) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sq = smem + L::q_off;
-  uint8_t* sop = smem + L::op_off;
-  uint8_t* sst = smem + L::st_off;
+  uint8_t* sk = smem + L::k_off;
+  uint8_t* svo = smem + L::vop_off;
+  uint8_t* svs = smem + L::vst_off;
   float* ssc = reinterpret_cast<float*>(smem + L::sc_off);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
@@ -416,16 +572,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ngrp = nw <= 1 ? 1 : (nw == 2 ? 2 : 4);  // row groups; 4 / ngrp copies per row
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < L::kStSlots; ++s) {
-      mbar_init(&bars[B_ST_FULL + s], 1);
-      mbar_init(&bars[B_ST_EMPTY + s], 4);
+    for (int s = 0; s < L::kKSlots; ++s) {
+      mbar_init(&bars[B_K_FULL + s], 1);
+      mbar_init(&bars[B_K_EMPTY + s], 5);
     }
-    for (int o = 0; o < kOpSlots; ++o) {
-      mbar_init(&bars[B_OP_FULL + o], 4);
-      mbar_init(&bars[B_OP_EMPTY + o], 1);
+    for (int s = 0; s < L::kVStSlots; ++s) {
+      mbar_init(&bars[B_VS_FULL + s], 1);
+      mbar_init(&bars[B_VS_EMPTY + s], 4);
+    }
+    for (int o = 0; o < kVOpSlots; ++o) {
+      mbar_init(&bars[B_VO_FULL + o], 4);
+      mbar_init(&bars[B_VO_EMPTY + o], 1);
     }
     for (int c = 0; c < kScSlots; ++c) {
-      mbar_init(&bars[B_SCK_FULL + c], 4);
       mbar_init(&bars[B_SCV_FULL + c], 4);
       mbar_init(&bars[B_SC_EMPTY + c], 4);
     }
@@ -436,6 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[B_RED_FULL + 0], 4);
     mbar_init(&bars[B_RED_FULL + 1], 4);
     mbar_init(&bars[B_EPI_FULL], 4);
+    mbar_init(&bars[B_Q_READY], 4);
     mbar_init(&bars[B_MMA_DONE], 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -443,28 +603,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 9) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
-  }
-  // Q tile (f16, K-major, 128-byte swizzle). TMEM lane 32w + l holds row
-  // 32 (w % ngrp) + l; lanes without a row are zero.
-  {
-    const uint4* q = static_cast<const uint4*>(a.q);
-    constexpr int CH = D / 8;  // 16-byte chunks per row
-    for (int idx = threadIdx.x; idx < BM * CH; idx += kThreads) {
-      const int r = idx / CH, c = idx - r * CH;
-      const int src = 32 * ((r >> 5) % ngrp) + (r & 31);
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (src < nr) {
-        const RowDesc rd = a.rows[it.row_begin + src];
-        const uint4 b = __ldg(q + ((int64_t)rd.q_index * a.n_q_heads + rd.q_head) * CH + c);
-        v.x = bf16x2_to_f16x2(b.x);
-        v.y = bf16x2_to_f16x2(b.y);
-        v.z = bf16x2_to_f16x2(b.z);
-        v.w = bf16x2_to_f16x2(b.w);
-      }
-      const int half = c >> 3, c8 = c & 7;
-      *reinterpret_cast<uint4*>(sq + half * L::kHalfBytes + r * 128 + ((c8 ^ (r & 7)) << 4)) = v;
-    }
-    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -478,145 +616,188 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t* btrow = a.block_table + (int64_t)it.bt_row * a.max_blocks;
     const int last_block = (it.k_end - 1) >> ps_shift;
     const int first_block = it.k_begin >> ps_shift;  // k_begin is page-aligned
-    int64_t my_row = 0;  // first cache row of this lane's page (rows of D codes)
-    int issued = 0;
-    for (int i = 0; i < 2 * n; ++i) {
-      const int j = i >> 1, s = i % L::kStSlots;
-      const uint32_t ph = (uint32_t)(i / L::kStSlots) & 1u;
-      if (i >= L::kStSlots &&
-          !__all_sync(0xffffffffu, mbar_wait(&bars[B_ST_EMPTY + s], ph ^ 1u, abort_flag,
+    // lane < npg owns one page of every tile. Its block-table entry is
+    // loaded one K tile ahead (the load completes while the items before
+    // that tile are issued); V_j reuses K_j's page, issued after K_(j+1)
+    // except for the last tile.
+    auto page_of = [&](int j) -> int32_t {
+      int b = first_block + j * npg + lane;
+      if (b > last_block) b = last_block;  // keys past k_end: masked, V zeroed
+      return __ldg(btrow + b);
+    };
+    auto row_of = [&](int32_t page) -> int64_t {  // first cache row of the page
+      if ((unsigned)page >= (unsigned)a.num_pages) {
+        set_status(a.status, MB_ERR_DEVICE_INDEX);
+        page = 0;
+      }
+      return ((int64_t)page * a.n_kv_heads + it.kv_head) << ps_shift;
+    };
+    int32_t next_page = lane < npg ? page_of(0) : 0;
+    int64_t cur_row = 0, prev_row = 0;  // tiles of the latest and the previous K item
+    int nk = 0, nv = 0;                 // K / V tiles issued
+    for (int s = 0; s < 2 * n; ++s) {
+      const SeqItem si = seq_item(s, n);
+      const int j = si.j;
+      const int slot = si.v ? j % L::kVStSlots : j % L::kKSlots;
+      if (!si.v && j >= L::kKSlots &&
+          !__all_sync(0xffffffffu, mbar_wait(&bars[B_K_EMPTY + slot],
+                                             ((uint32_t)(j / L::kKSlots) & 1u) ^ 1u, abort_flag,
                                              a.status)))
         break;
-      if ((i & 1) == 0 && lane < npg) {
-        int b = first_block + j * npg + lane;
-        if (b > last_block) b = last_block;  // keys past k_end: masked, V zeroed
-        int32_t page = __ldg(btrow + b);
-        if ((unsigned)page >= (unsigned)a.num_pages) {
-          set_status(a.status, MB_ERR_DEVICE_INDEX);
-          page = 0;
+      if (si.v && j >= L::kVStSlots &&
+          !__all_sync(0xffffffffu, mbar_wait(&bars[B_VS_EMPTY + slot],
+                                             ((uint32_t)(j / L::kVStSlots) & 1u) ^ 1u,
+                                             abort_flag, a.status)))
+        break;
+      int64_t my_row = 0;  // first cache row of this lane's page (rows of D codes)
+      if (lane < npg) {
+        if (!si.v) {
+          prev_row = cur_row;
+          cur_row = row_of(next_page);
+          if (j + 1 < n) next_page = page_of(j + 1);
+          my_row = cur_row;
+        } else {
+          my_row = j == nk - 1 ? cur_row : prev_row;
         }
-        my_row = ((int64_t)page * a.n_kv_heads + it.kv_head) << ps_shift;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&bars[B_ST_FULL + s], L::kStBytes);
+      uint64_t* full = &bars[(si.v ? B_VS_FULL : B_K_FULL) + slot];
+      if (lane == 0) mbar_arrive_expect_tx(full, L::kCodes + BN * 4);
       __syncwarp();
       if (lane < npg) {
-        uint8_t* dst = sst + s * L::kStBytes;
-        const uint8_t* codes = static_cast<const uint8_t*>((i & 1) ? a.v8 : a.k8);
-        const float* scales = (i & 1) ? a.v_scale : a.k_scale;
-        bulk_load(dst + lane * ps * D, codes + my_row * D, (uint32_t)(ps * D),
-                  &bars[B_ST_FULL + s]);
-        bulk_load(dst + L::kStCodes + lane * ps * 4, scales + my_row, (uint32_t)(ps * 4),
-                  &bars[B_ST_FULL + s]);
+        if (!si.v) {
+          uint8_t* dst = sk + slot * L::kKSlot;
+          tma_load_2d(dst + lane * ps * D, &k_map, full, 0, (int32_t)my_row);
+          bulk_load(dst + L::kCodes + lane * ps * 4, a.k_scale + my_row, (uint32_t)(ps * 4), full);
+        } else {
+          uint8_t* dst = svs + slot * L::kVStBytes;
+          bulk_load(dst + lane * ps * D, static_cast<const uint8_t*>(a.v8) + my_row * D,
+                    (uint32_t)(ps * D), full);
+          bulk_load(dst + L::kCodes + lane * ps * 4, a.v_scale + my_row, (uint32_t)(ps * 4), full);
+        }
       }
-      issued = i + 1;
+      if (si.v)
+        ++nv;
+      else
+        ++nk;
     }
     __syncwarp();
-    if (lane == 0)
-      for (int i = max(0, issued - L::kStSlots); i < issued; ++i)
-        mbar_drain(&bars[B_ST_FULL + i % L::kStSlots], (uint32_t)(i / L::kStSlots) & 1u,
+    if (lane == 0) {
+      for (int j = max(0, nk - L::kKSlots); j < nk; ++j)
+        mbar_drain(&bars[B_K_FULL + j % L::kKSlots], (uint32_t)(j / L::kKSlots) & 1u, kDrainNs);
+      for (int j = max(0, nv - L::kVStSlots); j < nv; ++j)
+        mbar_drain(&bars[B_VS_FULL + j % L::kVStSlots], (uint32_t)(j / L::kVStSlots) & 1u,
                    kDrainNs);
+    }
   } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ converters
+    // ------------------------------------------------------------ V converters
     const int ct = threadIdx.x - 128;
-    constexpr int TPR = D / 8;  // 8-code tasks per key row
-    for (int i = 0; i < 2 * n; ++i) {
-      const int j = i >> 1, s = i % L::kStSlots, o = i % kOpSlots, sc = j % kScSlots;
-      const bool is_v = i & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_ST_FULL + s],
-                                             (uint32_t)(i / L::kStSlots) & 1u, abort_flag,
+    constexpr int CPR = D / 16;       // 16-code chunks per key row
+    constexpr int TASKS = BN * CPR;   // per tile
+    for (int j = 0; j < n; ++j) {
+      const int vs = j % L::kVStSlots, vo = j % kVOpSlots, sc = j % kScSlots;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_VS_FULL + vs],
+                                             (uint32_t)(j / L::kVStSlots) & 1u, abort_flag,
                                              a.status)))
         break;
-      if (i >= kOpSlots &&
-          !__all_sync(0xffffffffu, mbar_wait(&bars[B_OP_EMPTY + o],
-                                             ((uint32_t)(i / kOpSlots) & 1u) ^ 1u, abort_flag,
+      if (j >= kVOpSlots &&
+          !__all_sync(0xffffffffu, mbar_wait(&bars[B_VO_EMPTY + vo],
+                                             ((uint32_t)(j / kVOpSlots) & 1u) ^ 1u, abort_flag,
                                              a.status)))
         break;
-      if (!is_v && j >= kScSlots &&
+      if (j >= kScSlots &&
           !__all_sync(0xffffffffu, mbar_wait(&bars[B_SC_EMPTY + sc],
                                              ((uint32_t)(j / kScSlots) & 1u) ^ 1u, abort_flag,
                                              a.status)))
         break;
       tc_fence_after();
-      const uint8_t* st = sst + s * L::kStBytes;
-      uint8_t* op = sop + o * L::kTileBytes;
+      const uint8_t* stg = svs + vs * L::kVStBytes;
+      const uint32_t stg_s = smem_u32(stg);
+      const uint32_t op_s = smem_u32(svo + vo * L::kVOpBytes);
       const int nvalid = min(BN, it.k_end - (it.k_begin + j * BN));
-      if (!is_v) {
-#pragma unroll 4
-        for (int idx = ct; idx < BN * TPR; idx += 128) {
-          const int key = idx / TPR, e8 = idx % TPR;
-          const uint2 raw = *reinterpret_cast<const uint2*>(st + key * D + e8 * 8);
-          uint4 v;
-          v.x = e4m3x2_to_f16x2(raw.x);
-          v.y = e4m3x2_to_f16x2(raw.x >> 16);
-          v.z = e4m3x2_to_f16x2(raw.y);
-          v.w = e4m3x2_to_f16x2(raw.y >> 16);
-          const int half = e8 >> 3, c8 = e8 & 7;
-          *reinterpret_cast<uint4*>(op + half * L::kHalfBytes + key * 128 +
-                                    ((c8 ^ (key & 7)) << 4)) = v;
-        }
-      } else {
-#pragma unroll 4
-        for (int idx = ct; idx < BN * TPR; idx += 128) {
-          const int key = idx / TPR, e8 = idx % TPR;
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (key < nvalid) {  // rows past k_end may hold any bits (P is 0 there)
-            const uint2 raw = *reinterpret_cast<const uint2*>(st + key * D + e8 * 8);
-            v.x = f16x2_to_bf16x2(e4m3x2_to_f16x2(raw.x));
-            v.y = f16x2_to_bf16x2(e4m3x2_to_f16x2(raw.x >> 16));
-            v.z = f16x2_to_bf16x2(e4m3x2_to_f16x2(raw.y));
-            v.w = f16x2_to_bf16x2(e4m3x2_to_f16x2(raw.y >> 16));
-          }
-          const int half = e8 >> 3, c8 = e8 & 7;
-          *reinterpret_cast<uint4*>(op + half * L::kHalfBytes + key * 128 +
-                                    ((c8 ^ (key & 7)) << 4)) = v;
-        }
+      // task t: key t / CPR, codes [16 q, 16 q + 16) -> f16 chunks 2q', 2q'+1
+      // of half q / 4 (q' = q % 4 for D = 128). The lanes of a store phase
+      // hit distinct banks: for D = 128 lanes with q >= 4 store their second
+      // chunk first; for D = 64 the phase's two keys swizzle apart.
+#pragma unroll
+      for (int t = ct; t < TASKS; t += 128) {
+        const int key = t / CPR, q = t % CPR;
+        uint4 raw = lds4u(stg_s + key * D + q * 16);
+        if (key >= nvalid) raw = make_uint4(0u, 0u, 0u, 0u);  // rows past k_end
+        const bool swap = D == 128 && q >= 4;
+        const uint32_t w0 = swap ? raw.z : raw.x, w1 = swap ? raw.w : raw.y;
+        const uint32_t w2 = swap ? raw.x : raw.z, w3 = swap ? raw.y : raw.w;
+        uint4 first, second;
+        first.x = e4m3x2_to_f16x2(w0);
+        first.y = e4m3x2_to_f16x2(w0 >> 16);
+        first.z = e4m3x2_to_f16x2(w1);
+        first.w = e4m3x2_to_f16x2(w1 >> 16);
+        second.x = e4m3x2_to_f16x2(w2);
+        second.y = e4m3x2_to_f16x2(w2 >> 16);
+        second.z = e4m3x2_to_f16x2(w3);
+        second.w = e4m3x2_to_f16x2(w3 >> 16);
+        const int half = D == 128 ? (q >> 2) : 0;
+        const int c0 = 2 * (D == 128 ? (q & 3) : q);
+        const int sw = key & 7;
+        const uint32_t rowp = op_s + half * L::kHalfBytes + key * 128;
+        sts4u(rowp + (((c0 + (swap ? 1 : 0)) ^ sw) << 4), first);
+        sts4u(rowp + (((c0 + (swap ? 0 : 1)) ^ sw) << 4), second);
       }
       {
-        const float x = reinterpret_cast<const float*>(st + L::kStCodes)[ct];
-        float* dst = ssc + sc * 2 * BN + (is_v ? BN : 0);
-        dst[ct] = is_v ? (ct < nvalid ? x : 0.f) : x * a.scale_log2;
+        // key ct's scale (0 past k_end) and the largest of this warp's 32
+        float v = lds1(stg_s + L::kCodes + 4 * ct);
+        if (ct >= nvalid) v = 0.f;
+        float* dst = ssc + sc * kScFloats;
+        dst[ct] = v;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+        if (lane == 0) dst[BN + (warp - 4)] = v;
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&bars[B_ST_EMPTY + s]);
-        mbar_arrive(&bars[B_OP_FULL + o]);
-        mbar_arrive(&bars[(is_v ? B_SCV_FULL : B_SCK_FULL) + sc]);
+        mbar_arrive(&bars[B_VS_EMPTY + vs]);
+        mbar_arrive(&bars[B_VO_FULL + vo]);
+        mbar_arrive(&bars[B_SCV_FULL + sc]);
       }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      // with kind::f8f6f4 format code 0 is e4m3: S = (hi | lo)(e4m3) x K(e4m3)
       constexpr uint32_t idesc_qk = idesc_f16_f32(BM, BN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
-      const uint32_t qa = smem_u32(sq);
-      const uint32_t opa = smem_u32(sop);
+      constexpr uint32_t idesc_pv = idesc_f16_f32(BM, D, false, true);
+      const uint32_t ka = smem_u32(sk);
+      const uint32_t voa = smem_u32(svo);
       auto wait = [&](int b, uint32_t parity) -> bool {
         const bool ok = mbar_wait(&bars[b], parity, abort_flag, a.status);
         tc_fence_after();
         return ok;
       };
       auto issue_s = [&](int j) -> bool {
-        const int ki = 2 * j, o = ki % kOpSlots;
-        if (!wait(B_OP_FULL + o, (uint32_t)(ki / kOpSlots) & 1u)) return false;
-        const uint32_t k0 = opa + o * L::kTileBytes;
+        const int slot = j % L::kKSlots;
+        if (!wait(B_K_FULL + slot, (uint32_t)(j / L::kKSlots) & 1u)) return false;
+        const uint32_t k0 = ka + slot * L::kKSlot;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-          umma_bf16_ss(tmem + kColS + 128 * (j & 1), sdesc_sw128(qa + off, 16, 1024),
-                       sdesc_sw128(k0 + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-        }
+        for (int part = 0; part < 2; ++part)  // hi codes, then lo codes of Q
+#pragma unroll
+          for (int kk = 0; kk < D / 32; ++kk) {  // 32 e4m3 values (32 bytes) per MMA
+            const uint64_t bd = D == 128 ? sdesc_sw128(k0 + kk * 32, 16, 1024)
+                                         : sdesc_sw64(k0 + kk * 32, 16, 512);
+            umma_f8_ts(tmem + kColS + 128 * (j & 1), tmem + kColQ + part * (D / 4) + kk * 8, bd,
+                       idesc_qk, (part | kk) ? 1u : 0u);
+          }
         umma_commit(&bars[B_S_FULL + (j & 1)]);
-        umma_commit(&bars[B_OP_EMPTY + o]);
+        umma_commit(&bars[B_K_EMPTY + slot]);
         return true;
       };
-      bool ok = n > 0 && issue_s(0);
+      bool ok = n > 0 && wait(B_Q_READY, 0u);
+      if (ok) ok = issue_s(0);
       if (ok && n > 1) ok = issue_s(1);
       for (int j = 0; ok && j < n; ++j) {
-        const int vi = 2 * j + 1, o = vi % kOpSlots;
-        if (!(ok = wait(B_OP_FULL + o, (uint32_t)(vi / kOpSlots) & 1u))) break;
+        const int vo = j % kVOpSlots;
+        if (!(ok = wait(B_VO_FULL + vo, (uint32_t)(j / kVOpSlots) & 1u))) break;
         if (!(ok = wait(B_P_FULL, (uint32_t)j & 1u))) break;
-        const uint32_t v0 = opa + o * L::kTileBytes;
+        const uint32_t v0 = voa + vo * L::kVOpBytes;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint64_t bd = sdesc_sw128(v0 + kk * 2048, L::kHalfBytes, 1024);
@@ -624,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        (j > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&bars[B_O_DONE]);
-        umma_commit(&bars[B_OP_EMPTY + o]);
+        umma_commit(&bars[B_VO_EMPTY + vo]);
         // S(j+2) reuses this S buffer; it follows PV(j) in issue order
         if (j + 2 < n && !(ok = issue_s(j + 2))) break;
       }
@@ -637,10 +818,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     Shared sh;
     sh.bars = bars;
     sh.abort_flag = abort_flag;
+    sh.kring = sk;
     sh.sc = ssc;
     sh.redm = reinterpret_cast<float*>(smem + L::redm_off);
     sh.redl = reinterpret_cast<float*>(smem + L::redl_off);
-    sh.redo = reinterpret_cast<float*>(sop);
+    sh.redo = reinterpret_cast<float*>(sk);
     sh.tmem = tmem;
     if (ngrp == 1)
       softmax_role<D, 32>(a, it, sh, n, warp, lane);
@@ -669,13 +851,15 @@ cudaError_t launch_decode_fp8(const DecodeFp8Args& a, cudaStream_t s) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)Layout<128>::kAlloc);
     if (e != cudaSuccess) return e;
-    splitkv_fp8_kernel<128><<<(unsigned)a.n_items, kThreads, Layout<128>::kAlloc, s>>>(a, ps_shift);
+    splitkv_fp8_kernel<128><<<(unsigned)a.n_items, kThreads, Layout<128>::kAlloc, s>>>(
+        a, ps_shift, *a.k_map);
     return cudaGetLastError();
   }
   e = cudaFuncSetAttribute(splitkv_fp8_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)Layout<64>::kAlloc);
   if (e != cudaSuccess) return e;
-  splitkv_fp8_kernel<64><<<(unsigned)a.n_items, kThreads, Layout<64>::kAlloc, s>>>(a, ps_shift);
+  splitkv_fp8_kernel<64><<<(unsigned)a.n_items, kThreads, Layout<64>::kAlloc, s>>>(
+      a, ps_shift, *a.k_map);
   return cudaGetLastError();
 }
 

@@ -72,6 +72,7 @@ struct DecodeFp8Args {
   float* part_o;
   float* part_lse;
   int32_t* status;
+  const CUtensorMap* k_map;  // uint8 codes [rows, D], box D x ps, swizzled (host copy)
 };
 cudaError_t launch_decode_fp8(const DecodeFp8Args& a, cudaStream_t s);
 
