@@ -10,17 +10,17 @@
 // final rows or normalised partials for the combine kernel.
 //
 // The scales of key j factor out of both products:
-//   S[r][j] = ks_j sq_r (qc_r . kcode_j)    O[r] = rho sum_j (p[r][j] vs_j / rho) vcode_j
+//   S[r][j] = ks_j sq_r (qc_r . kcode_j)    O[r] = rho sum_j p[r][j] (vs_j / rho) vcode_j
 //   * Q K^T runs on the raw e4m3 K codes (kind::f8f6f4, fp32 accumulation):
 //     each query row q is written as sq (hi + lo) with sq = amax|q| / 448,
 //     hi = e4m3(q / sq) and lo = e4m3(q / sq - hi), two e4m3 rows whose
 //     products with the K tile add up in the same accumulator. hi + lo holds
 //     q to about 2^-8 of each value (near bf16's 2^-9), so the split costs
 //     the scores about what bf16 Q costs them, and no K value is converted.
-//   * P' V runs on f16 operands (every e4m3 value is exact in f16), with
-//     P' = p vs_j / rho. rho is a power of two at least as large as every V
-//     scale seen so far; it only grows, and O is rescaled by the exact ratio
-//     when it does, so P' stays within [0, 2^8] whatever the magnitude of V.
+//   * P V' runs on f16 operands: V' = vcode_j (vs_j / rho) and P = p. rho is
+//     the smallest power of two at least as large as every V scale of the
+//     CTA's keys, so V' stays within +-448 whatever the magnitude of V, and
+//     O = rho (P V') / l.
 //   The softmax applies ks_j sq_r (times log2(e) and the softmax scale) to
 //   the scores.
 //
@@ -31,10 +31,10 @@
 //               K-major operand layout of a 6-slot ring (8 for D = 64); V
 //               codes by bulk copy into a staging ring; each page's ps scales
 //               by bulk copy beside them.
-//   warps 4-7   V converters: 16 staged codes -> 8 f16x2 words per task into
-//               the operand tiles of a 2-slot ring (rows past k_end zeroed);
-//               the V scales and their largest value go to a small ring the
-//               softmax reads.
+//   warps 4-7   V converters: first the item's largest V scale (read from
+//               the scale array) sets rho; then 16 staged codes -> 8 f16x2
+//               words per task, times the key's vs / rho, into the operand
+//               tiles of a 2-slot ring (rows past k_end zeroed).
 //   warp 9      TMEM allocation; one lane issues S = Q K^T (the hi and lo
 //               rows of Q from TMEM) and O += P' V (P' from TMEM).
 //   warps 0-3   softmax; each thread first writes its query row's hi / lo
@@ -42,9 +42,9 @@
 //               each row is copied into 4 (or 2) TMEM lanes of different
 //               warps and each copy handles 32 (or 64) of the tile's 128
 //               keys, so the exponentials of one row spread over the 4 SM
-//               sub-partitions; the copies agree on the running max through
-//               shared memory every tile and add their partial sums and
-//               outputs at the end.
+//               sub-partitions. Each copy keeps its own running max, sum and
+//               accumulator (a split-KV partition of the row's keys); the
+//               epilogue merges them.
 // Every wait is bounded; on a timeout the CTA raises its abort flag, drains
 // what it issued, frees its TMEM and returns.
 #include <cuda_runtime.h>
@@ -69,8 +69,6 @@ constexpr uint32_t kColQ = 384;  // hi codes (D / 4 columns), then lo codes
 constexpr float kRescaleThreshold = 8.0f;
 constexpr uint64_t kDrainNs = 200000000ull;
 constexpr int kVOpSlots = 2;          // f16 V operand tiles
-constexpr int kScSlots = 4;           // per-tile V scale vectors
-constexpr int kScFloats = BN + 4;     // vs [BN], max vs per converter warp
 constexpr int kMaxSlots = 8;
 
 enum {
@@ -80,13 +78,11 @@ enum {
   B_VS_EMPTY = B_VS_FULL + kMaxSlots,    // + V staging slot
   B_VO_FULL = B_VS_EMPTY + kMaxSlots,    // + V operand slot
   B_VO_EMPTY = B_VO_FULL + kVOpSlots,    // + V operand slot
-  B_SCV_FULL = B_VO_EMPTY + kVOpSlots,   // + scale slot
-  B_SC_EMPTY = B_SCV_FULL + kScSlots,    // + scale slot
-  B_S_FULL = B_SC_EMPTY + kScSlots,      // + S buffer
+  B_S_FULL = B_VO_EMPTY + kVOpSlots,     // + S buffer
   B_P_FULL = B_S_FULL + 2,
   B_O_DONE = B_P_FULL + 1,
-  B_RED_FULL = B_O_DONE + 1,             // + buffer
-  B_EPI_FULL = B_RED_FULL + 2,
+  B_RHO_READY = B_O_DONE + 1,            // converters' partial maxima of the V scales
+  B_EPI_FULL = B_RHO_READY + 1,
   B_Q_READY = B_EPI_FULL + 1,
   B_MMA_DONE = B_Q_READY + 1,
   B_COUNT = B_MMA_DONE + 1
@@ -106,12 +102,12 @@ struct Layout {
   static constexpr uint32_t k_off = 0;
   static constexpr uint32_t vop_off = k_off + kKSlots * kKSlot;
   static constexpr uint32_t vst_off = vop_off + kVOpSlots * kVOpBytes;
-  static constexpr uint32_t sc_off = vst_off + kVStSlots * kVStBytes;
-  static constexpr uint32_t redm_off = sc_off + kScSlots * kScFloats * 4;  // float [2][4][32]
-  static constexpr uint32_t redl_off = redm_off + 2 * 4 * 32 * 4;           // float [4][32]
+  static constexpr uint32_t redm_off = vst_off + kVStSlots * kVStBytes;  // float [4][32]
+  static constexpr uint32_t redl_off = redm_off + 4 * 32 * 4;             // float [4][32]
   static constexpr uint32_t bar_off = redl_off + 4 * 32 * 4;
+  // TMEM address, abort flag, the converters' 4 partial maxima of the V scales
   static constexpr uint32_t misc_off = bar_off + B_COUNT * 8;
-  static constexpr uint32_t kBytes = misc_off + 16;
+  static constexpr uint32_t kBytes = misc_off + 32;
   // more than half the SM so that one CTA holds the SM's 512 TMEM columns
   static constexpr uint32_t kAlloc =
       (kBytes + 1024 > 232448u / 2 + 1024) ? kBytes + 1024 : 232448u / 2 + 1024;
@@ -120,6 +116,7 @@ struct Layout {
   static_assert(kKSlots <= kMaxSlots && kVStSlots <= kMaxSlots, "rings");
   static_assert(4 * 32 * kRedRow * 4 <= kKSlots * kKSlot, "reduction buffer");
   static_assert(kAlloc <= 232448, "shared memory");
+  static_assert(misc_off % 16 == 0, "misc alignment");
 };
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -157,6 +154,11 @@ __device__ __forceinline__ void f16x2_to_f32x2(uint32_t h, float& lo, float& hi)
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
 // Smallest power of two >= x, for finite x > 0.
@@ -211,16 +213,26 @@ struct Shared {
   uint64_t* bars;
   volatile int* abort_flag;
   const uint8_t* kring;  // K slots (codes, then scales)
-  const float* sc;       // [kScSlots][kScFloats]
-  float* redm;           // [2][4][32]
+  const float* rho4;     // the converters' 4 partial maxima of the V scales
+  float* redm;           // [4][32]
   float* redl;           // [4][32]
   float* redo;           // [4][32][D + 4] (K ring, epilogue only)
   uint32_t tmem;
 };
 
+// rho: the smallest power of two >= every V scale of the item (0 when all
+// are 0), from the converters' partial maxima.
+__device__ __forceinline__ float rho_of(const float* rho4) {
+  const float4 v = lds4(smem_u32(rho4));
+  const float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+  return mx > 0.f ? pow2_ceil(mx) : 0.f;
+}
+
 // Softmax role of warp `warp` (0-3). Rows: group g = warp % ngrp of 32 rows,
 // copy c = warp / ngrp; W = 128 / R keys of every tile per copy (R = 4 / ngrp
-// copies of each row).
+// copies of each row). Each copy runs its own online softmax over its keys
+// (its own running max m, sum l and TMEM accumulator lane): the copies of a
+// row are split-KV partitions by key, merged in the epilogue.
 template <int D, int W>
 __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const DecodeItem& it,
                                              const Shared& sh, int n, int warp, int lane) {
@@ -291,13 +303,9 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
   const int col0 = c * W;
   const float crow = a.scale_log2 * sq;  // this row's factor of every score
   float m = -INFINITY, l = 0.f;
-  float rho = 0.f, inv_rho = 0.f;  // V-scale reference (power of two), its inverse
   bool ok = true;
   for (int j = 0; j < n; ++j) {
-    const int sc = j % kScSlots;
-    const uint32_t scph = (uint32_t)(j / kScSlots) & 1u;
     const int ks_slot = j % L::kKSlots;
-    const float* scv = sh.sc + sc * kScFloats;
     const uint32_t p_col = sh.tmem + lane_addr + kColS + 128 * (j & 1);
     ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_S_FULL + (j & 1)], (uint32_t)(j >> 1) & 1u,
                                            sh.abort_flag, a.status));
@@ -340,19 +348,6 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
 #pragma unroll
       for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(x[e]));
     }
-    if constexpr (R > 1) {
-      // the copies of a row agree on the tile max
-      float* red = sh.redm + (j & 1) * 128;
-      red[warp * 32 + lane] = mx;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_RED_FULL + (j & 1)]);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_RED_FULL + (j & 1)],
-                                             (uint32_t)(j >> 1) & 1u, sh.abort_flag, a.status));
-      if (!ok) break;
-#pragma unroll
-      for (int cc = 0; cc < R; ++cc)
-        mx = fmaxf(mx, lds1(smem_u32(red + (g + ngrp * cc) * 32 + lane)));
-    }
     const float m_new = fmaxf(m, mx);
     float alpha = 1.f;
     bool need = false;
@@ -365,28 +360,9 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
       m = m_new;
     }
     const float mc = (m == -INFINITY) ? 0.f : m;
-    ok = __all_sync(0xffffffffu,
-                    mbar_wait(&bars[B_SCV_FULL + sc], scph, sh.abort_flag, a.status));
-    if (!ok) break;
-    // the V-scale reference grows (by an exact power of two) to cover this
-    // tile's largest scale; the same for every thread of the CTA
-    {
-      const float4 v4 = lds4(smem_u32(scv + BN));
-      const float vmx = fmaxf(fmaxf(v4.x, v4.y), fmaxf(v4.z, v4.w));
-      if (vmx > rho) {
-        const float nr = pow2_ceil(vmx);
-        if (rho > 0.f) {
-          alpha *= rho / nr;
-          need = true;
-        }
-        rho = nr;
-        inv_rho = 1.f / nr;
-      }
-    }
-    // P' = p * vs_j / rho in f16, stored 16 packed columns (32 keys) at a
-    // time into S buffer j & 1 (P(j-1) V(j-1) reads the other one); the
+    // P = p in f16 (V carries vs / rho), stored 16 packed columns (32 keys)
+    // at a time into S buffer j & 1 (P(j-1) V(j-1) reads the other one); the
     // other copies' columns are zero
-    const uint32_t vf = smem_u32(scv + col0);
     float sum[2] = {0.f, 0.f};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -399,15 +375,14 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
         if (W > 64) scaled_chunk(h, x);
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 f = lds4(vf + 16 * (8 * h + e4));
           const float p0 = fast_exp2(__uint_as_float(x[4 * e4]) - mc);
           const float p1 = fast_exp2(__uint_as_float(x[4 * e4 + 1]) - mc);
           const float p2 = fast_exp2(__uint_as_float(x[4 * e4 + 2]) - mc);
           const float p3 = fast_exp2(__uint_as_float(x[4 * e4 + 3]) - mc);
           sum[0] += p0 + p2;
           sum[1] += p1 + p3;
-          pk[2 * e4] = pack_f16x2(p0 * (f.x * inv_rho), p1 * (f.y * inv_rho));
-          pk[2 * e4 + 1] = pack_f16x2(p2 * (f.z * inv_rho), p3 * (f.w * inv_rho));
+          pk[2 * e4] = pack_f16x2(p0, p1);
+          pk[2 * e4 + 1] = pack_f16x2(p2, p3);
         }
       } else {
 #pragma unroll
@@ -417,10 +392,7 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
     }
     l += sum[0] + sum[1];
     __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(&bars[B_SC_EMPTY + sc]);
-      mbar_arrive(&bars[B_K_EMPTY + ks_slot]);  // done with the K tile's scales
-    }
+    if (lane == 0) mbar_arrive(&bars[B_K_EMPTY + ks_slot]);  // done with the K tile's scales
     // O may be rescaled once P(j-1) V(j-1) completed; waiting every tile
     // also keeps this barrier's phases in step
     if (j > 0) {
@@ -448,8 +420,12 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
   if (ok && n > 0)
     ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE], (uint32_t)(n - 1) & 1u,
                                            sh.abort_flag, a.status));
+  // the V operand carries vs / rho: O = rho * (P V') / l
+  if (ok && n > 0)
+    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_RHO_READY], 0u, sh.abort_flag, a.status));
   if (!ok || n == 0) return;
   tc_fence_after();
+  const float rho = rho_of(sh.rho4);
   const bool final_row = rd.dst < 0;
   const int64_t orow = (int64_t)rd.q_index * a.n_q_heads + rd.q_head;
   if constexpr (R == 1) {
@@ -485,10 +461,12 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
     if (valid && final_row && a.lse) a.lse[orow] = lse2 * 0.6931471805599453f;
     if (valid && !final_row) a.part_lse[rd.dst] = lse2;
   } else {
-    // add the R copies: every warp parks its lanes' l and O, then finishes
-    // D / R columns of its row group
+    // merge the R copies (split-KV partitions of the row's keys): every warp
+    // parks its lanes' m, l and O, then finishes D / R columns of its row
+    // group with weights 2^(m_c - M), M the largest m_c
     constexpr int RR = L::kRedRow;
     sh.redl[warp * 32 + lane] = l;
+    sh.redm[warp * 32 + lane] = m;
     float* mine = sh.redo + (warp * 32 + lane) * RR;
 #pragma unroll
     for (int cc = 0; cc < D / 32; ++cc) {
@@ -505,12 +483,22 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
     if (lane == 0) mbar_arrive(&bars[B_EPI_FULL]);
     if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_EPI_FULL], 0u, sh.abort_flag, a.status)))
       return;
+    float mcp[R], wc[R];
+    float M = -INFINITY;
+#pragma unroll
+    for (int cc = 0; cc < R; ++cc) {
+      mcp[cc] = lds1(smem_u32(sh.redm + (g + ngrp * cc) * 32 + lane));
+      M = fmaxf(M, mcp[cc]);
+    }
     float lt = 0.f;
 #pragma unroll
-    for (int cc = 0; cc < R; ++cc) lt += lds1(smem_u32(sh.redl + (g + ngrp * cc) * 32 + lane));
+    for (int cc = 0; cc < R; ++cc) {
+      wc[cc] = M == -INFINITY ? 0.f : fast_exp2(mcp[cc] - M);  // 0 for a copy with no key
+      lt += wc[cc] * lds1(smem_u32(sh.redl + (g + ngrp * cc) * 32 + lane));
+    }
     const bool any = lt > 0.f;
     const float inv = any ? rho / lt : 0.f;
-    const float lse2 = any ? m + log2f(lt) : -INFINITY;
+    const float lse2 = any ? M + log2f(lt) : -INFINITY;
     constexpr int CW = D / R;  // columns this warp finishes
     const int cbeg = c * CW;
     if (valid) {
@@ -521,10 +509,10 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
 #pragma unroll
         for (int cc = 0; cc < R; ++cc) {
           const float4 v = lds4(smem_u32(sh.redo + ((g + ngrp * cc) * 32 + lane) * RR + col));
-          acc.x += v.x;
-          acc.y += v.y;
-          acc.z += v.z;
-          acc.w += v.w;
+          acc.x = fmaf(wc[cc], v.x, acc.x);
+          acc.y = fmaf(wc[cc], v.y, acc.y);
+          acc.z = fmaf(wc[cc], v.z, acc.z);
+          acc.w = fmaf(wc[cc], v.w, acc.w);
         }
         if (final_row) {
           uint2 w;
@@ -555,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sk = smem + L::k_off;
   uint8_t* svo = smem + L::vop_off;
   uint8_t* svs = smem + L::vst_off;
-  float* ssc = reinterpret_cast<float*>(smem + L::sc_off);
+  float* rho4 = reinterpret_cast<float*>(smem + L::misc_off + 16);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
@@ -584,16 +572,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[B_VO_FULL + o], 4);
       mbar_init(&bars[B_VO_EMPTY + o], 1);
     }
-    for (int c = 0; c < kScSlots; ++c) {
-      mbar_init(&bars[B_SCV_FULL + c], 4);
-      mbar_init(&bars[B_SC_EMPTY + c], 4);
-    }
     mbar_init(&bars[B_S_FULL + 0], 1);
     mbar_init(&bars[B_S_FULL + 1], 1);
     mbar_init(&bars[B_P_FULL], 4);
     mbar_init(&bars[B_O_DONE], 1);
-    mbar_init(&bars[B_RED_FULL + 0], 4);
-    mbar_init(&bars[B_RED_FULL + 1], 4);
+    mbar_init(&bars[B_RHO_READY], 4);
     mbar_init(&bars[B_EPI_FULL], 4);
     mbar_init(&bars[B_Q_READY], 4);
     mbar_init(&bars[B_MMA_DONE], 1);
@@ -693,8 +676,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ct = threadIdx.x - 128;
     constexpr int CPR = D / 16;       // 16-code chunks per key row
     constexpr int TASKS = BN * CPR;   // per tile
-    for (int j = 0; j < n; ++j) {
-      const int vs = j % L::kVStSlots, vo = j % kVOpSlots, sc = j % kScSlots;
+    // rho first: the largest V scale of the item's keys, read straight from
+    // the scale array (4 bytes per key, beside the 128 bytes of codes the
+    // producer is already fetching); each warp's maximum goes to shared
+    // memory, and every consumer takes the power of two >= the largest
+    {
+      const int ps = 1 << ps_shift;
+      const int32_t* btrow = a.block_table + (int64_t)it.bt_row * a.max_blocks;
+      const int last_block = (it.k_end - 1) >> ps_shift;
+      float vmx = 0.f;
+      for (int b = (it.k_begin >> ps_shift) + ct; b <= last_block; b += 128) {
+        const int32_t page = __ldg(btrow + b);
+        if ((unsigned)page >= (unsigned)a.num_pages) continue;  // flagged by the producer
+        const float4* sp = reinterpret_cast<const float4*>(
+            a.v_scale + (((int64_t)page * a.n_kv_heads + it.kv_head) << ps_shift));
+        const int nk = min(ps, it.k_end - (b << ps_shift));  // keys of the page below k_end
+#pragma unroll 4
+        for (int e4 = 0; e4 < ps / 4; ++e4) {
+          const float4 v = __ldg(sp + e4);
+          if (4 * e4 + 0 < nk) vmx = fmaxf(vmx, v.x);
+          if (4 * e4 + 1 < nk) vmx = fmaxf(vmx, v.y);
+          if (4 * e4 + 2 < nk) vmx = fmaxf(vmx, v.z);
+          if (4 * e4 + 3 < nk) vmx = fmaxf(vmx, v.w);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        vmx = fmaxf(vmx, __shfl_xor_sync(0xffffffffu, vmx, off));
+      if (lane == 0) rho4[warp - 4] = vmx;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_RHO_READY]);
+    }
+    const bool rho_ok =
+        __all_sync(0xffffffffu, mbar_wait(&bars[B_RHO_READY], 0u, abort_flag, a.status));
+    const float rho = rho_ok ? rho_of(rho4) : 0.f;
+    const float inv_rho = rho > 0.f ? 1.f / rho : 0.f;
+    for (int j = 0; rho_ok && j < n; ++j) {
+      const int vs = j % L::kVStSlots, vo = j % kVOpSlots;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_VS_FULL + vs],
                                              (uint32_t)(j / L::kVStSlots) & 1u, abort_flag,
                                              a.status)))
@@ -704,25 +722,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ((uint32_t)(j / kVOpSlots) & 1u) ^ 1u, abort_flag,
                                              a.status)))
         break;
-      if (j >= kScSlots &&
-          !__all_sync(0xffffffffu, mbar_wait(&bars[B_SC_EMPTY + sc],
-                                             ((uint32_t)(j / kScSlots) & 1u) ^ 1u, abort_flag,
-                                             a.status)))
-        break;
       tc_fence_after();
       const uint8_t* stg = svs + vs * L::kVStBytes;
       const uint32_t stg_s = smem_u32(stg);
       const uint32_t op_s = smem_u32(svo + vo * L::kVOpBytes);
       const int nvalid = min(BN, it.k_end - (it.k_begin + j * BN));
       // task t: key t / CPR, codes [16 q, 16 q + 16) -> f16 chunks 2q', 2q'+1
-      // of half q / 4 (q' = q % 4 for D = 128). The lanes of a store phase
-      // hit distinct banks: for D = 128 lanes with q >= 4 store their second
-      // chunk first; for D = 64 the phase's two keys swizzle apart.
+      // of half q / 4 (q' = q % 4 for D = 128), each value times the key's
+      // vs / rho (f16, at most 1). The lanes of a store phase hit distinct
+      // banks: for D = 128 lanes with q >= 4 store their second chunk first;
+      // for D = 64 the phase's two keys swizzle apart.
 #pragma unroll
       for (int t = ct; t < TASKS; t += 128) {
         const int key = t / CPR, q = t % CPR;
         uint4 raw = lds4u(stg_s + key * D + q * 16);
-        if (key >= nvalid) raw = make_uint4(0u, 0u, 0u, 0u);  // rows past k_end
+        const float fk = lds1(stg_s + L::kCodes + 4 * key) * inv_rho;
+        // rows past k_end (their bits, scale included, may be anything): 0
+        const uint32_t f2 = key < nvalid ? pack_f16x2(fk, fk) : 0u;
+        if (key >= nvalid) raw = make_uint4(0u, 0u, 0u, 0u);
         const bool swap = D == 128 && q >= 4;
         const uint32_t w0 = swap ? raw.z : raw.x, w1 = swap ? raw.w : raw.y;
         const uint32_t w2 = swap ? raw.x : raw.z, w3 = swap ? raw.y : raw.w;
@@ -735,6 +752,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         second.y = e4m3x2_to_f16x2(w2 >> 16);
         second.z = e4m3x2_to_f16x2(w3);
         second.w = e4m3x2_to_f16x2(w3 >> 16);
+        first.x = hmul2(first.x, f2);
+        first.y = hmul2(first.y, f2);
+        first.z = hmul2(first.z, f2);
+        first.w = hmul2(first.w, f2);
+        second.x = hmul2(second.x, f2);
+        second.y = hmul2(second.y, f2);
+        second.z = hmul2(second.z, f2);
+        second.w = hmul2(second.w, f2);
         const int half = D == 128 ? (q >> 2) : 0;
         const int c0 = 2 * (D == 128 ? (q & 3) : q);
         const int sw = key & 7;
@@ -742,22 +767,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         sts4u(rowp + (((c0 + (swap ? 1 : 0)) ^ sw) << 4), first);
         sts4u(rowp + (((c0 + (swap ? 0 : 1)) ^ sw) << 4), second);
       }
-      {
-        // key ct's scale (0 past k_end) and the largest of this warp's 32
-        float v = lds1(stg_s + L::kCodes + 4 * ct);
-        if (ct >= nvalid) v = 0.f;
-        float* dst = ssc + sc * kScFloats;
-        dst[ct] = v;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-        if (lane == 0) dst[BN + (warp - 4)] = v;
-      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&bars[B_VS_EMPTY + vs]);
         mbar_arrive(&bars[B_VO_FULL + vo]);
-        mbar_arrive(&bars[B_SCV_FULL + sc]);
       }
     }
   } else if (warp == 9) {
@@ -819,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sh.bars = bars;
     sh.abort_flag = abort_flag;
     sh.kring = sk;
-    sh.sc = ssc;
+    sh.rho4 = rho4;
     sh.redm = reinterpret_cast<float*>(smem + L::redm_off);
     sh.redl = reinterpret_cast<float*>(smem + L::redl_off);
     sh.redo = reinterpret_cast<float*>(sk);
