@@ -83,6 +83,21 @@ def parse_args(argv=None):
     return args
 
 
+def job_throughput(total_ms_local, rows_per_step, steps, world):
+    """Whole-job rate of `world` replicas that each timed `steps` steps of
+    `rows_per_step` rows: the job takes as long as its slowest rank (max over
+    ranks through the default process group when world > 1). Returns (rows/s,
+    job milliseconds)."""
+    total_ms = float(total_ms_local)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return world * rows_per_step * steps / (total_ms / 1e3), total_ms
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -500,12 +515,7 @@ def run_gpu(args):
                 sev[i][2 * si].elapsed_time(sev[i][2 * si + 1]) for i in range(K))
     stage_ms["append"] = statistics.mean(a.elapsed_time(b) for a, b in aev)
     ms_step = statistics.mean(step_ms)
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * w.total_q * K / (total_ms / 1e3)
+    value, total_ms = job_throughput(sum(step_ms), w.total_q, K, world)
     dev_status = int(ws[:4].view(torch.int32).item()) | int(status.item())
 
     # ---- roofline of the dominant kernel
