@@ -403,11 +403,13 @@ def run_gpu(args):
         else:
             B.kv_append(kc, vc, kn, vn, slot_t, cfg, status)
 
-    def forward(plan, q_t, events=None):
+    def forward(plan, q_t, events=None, o=None, l=None):
+        o = out if o is None else o
+        l = lse if l is None else l
         if args.fp8:
-            plan.forward_fp8(q_t, kc, vc, ksc, vsc, bt_dev, out, lse, events=events)
+            plan.forward_fp8(q_t, kc, vc, ksc, vsc, bt_dev, o, l, events=events)
         else:
-            plan.forward(q_t, kc, vc, bt_dev, out, lse, events=events)
+            plan.forward(q_t, kc, vc, bt_dev, o, l, events=events)
 
     n_hist = int(w.hist_requests[:, 1].max()) if w.n_requests else 0
     if n_hist:
@@ -585,13 +587,64 @@ def run_gpu(args):
             e2e_step()
             torch.cuda.synchronize()
             e_ms.append((time.perf_counter() - t0) * 1e3)
+
+        # A serving loop keeps steps in flight: step i's upload (its own
+        # stream) overlaps step i-1's attention, and its download (a third
+        # stream) overlaps step i+1's upload. Inputs and outputs rotate over
+        # NBUF buffer sets; every step still uploads its Q/K/V and downloads
+        # its O/LSE.
+        NBUF = 3
+        s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        bufs = [dict(q=torch.empty_like(q), k=torch.empty_like(k_new), v=torch.empty_like(v_new),
+                     o=torch.empty_like(out), l=torch.empty_like(lse),
+                     ho=torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+                     hl=torch.empty(lse.shape, dtype=lse.dtype).pin_memory(),
+                     free=torch.cuda.Event(), up=torch.cuda.Event(), done=torch.cuda.Event())
+                for _ in range(NBUF)]
+
+        def piped_step(i):
+            b = bufs[i % NBUF]
+            with torch.cuda.stream(s_up):
+                if i >= NBUF:  # step i-NBUF has been computed and downloaded
+                    s_up.wait_event(b["free"])
+                b["q"].copy_(hq, non_blocking=True)
+                b["k"].copy_(hk, non_blocking=True)
+                b["v"].copy_(hv, non_blocking=True)
+                b["up"].record(s_up)
+            stream.wait_event(b["up"])
+            append_rows(b["k"], b["v"], slots)
+            plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=ws, opts=opts)
+            forward(plan, b["q"], o=b["o"], l=b["l"])
+            plan.close()
+            b["done"].record(stream)
+            with torch.cuda.stream(s_down):
+                s_down.wait_event(b["done"])
+                b["ho"].copy_(b["o"], non_blocking=True)
+                b["hl"].copy_(b["l"], non_blocking=True)
+                b["free"].record(s_down)
+
+        for i in range(max(3, args.warmup)):
+            piped_step(i)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(K):
+            piped_step(i)
+        torch.cuda.synchronize()
+        piped_ms = (time.perf_counter() - t0) * 1e3 / K
         h2d = (hq.numel() + hk.numel() + hv.numel()) * 2 + info["metadata_bytes"]
         d2h = hout.numel() * 2 + hlse.numel() * 4
-        e2e = {"value": world * w.total_q / (statistics.mean(e_ms) / 1e3), "unit": UNIT,
+        e2e = {"value": world * w.total_q / (piped_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": statistics.mean(e_ms),
-               "timing": "host wall clock around each step, synchronised; inputs copied from "
-                         "pinned host memory, output and LSE copied back"}
+               "ms_per_step": piped_ms,
+               "timing": "K steps through the public calls, pipelined (each step's Q/K/V "
+                         "upload from pinned host memory on an upload stream, append + plan + "
+                         "forward on the compute stream, O/LSE download on a third stream; "
+                         "inputs and outputs rotate over 3 buffer sets); host wall clock over "
+                         "the K steps, synchronised at both ends",
+               "serial": {"value": world * w.total_q / (statistics.mean(e_ms) / 1e3),
+                          "ms_per_step": statistics.mean(e_ms),
+                          "timing": "one step at a time: host wall clock around each step, "
+                                    "synchronised, L2 flushed before it"}}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
