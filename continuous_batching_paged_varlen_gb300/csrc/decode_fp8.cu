@@ -66,6 +66,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // + 128 * buffer
 constexpr uint32_t kColO = 256;  // D columns
 constexpr uint32_t kColQ = 384;  // hi codes (D / 4 columns), then lo codes
+constexpr uint32_t kColP = 448;  // P: 64 columns of f16x2 (128 keys), kept between tiles
 constexpr float kRescaleThreshold = 8.0f;
 constexpr uint64_t kDrainNs = 200000000ull;
 constexpr int kVOpSlots = 2;          // f16 V operand tiles
@@ -292,6 +293,14 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
         tmem_st16(sh.tmem + lane_addr + kColQ + QW, lo);
       }
     }
+    // P starts as zeros; each copy then rewrites only its own keys' columns
+    {
+      uint32_t zero[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) zero[e] = 0u;
+      tmem_st32(sh.tmem + lane_addr + kColP, zero);
+      tmem_st32(sh.tmem + lane_addr + kColP + 32, zero);
+    }
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
@@ -300,6 +309,7 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
 
   const int vis_hi = min(it.k_end, rd.vis_end);
   const uint32_t o_col = sh.tmem + lane_addr + kColO;
+  const uint32_t p_base = sh.tmem + lane_addr + kColP;
   const int col0 = c * W;
   const float crow = a.scale_log2 * sq;  // this row's factor of every score
   float m = -INFINITY, l = 0.f;
@@ -360,47 +370,55 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
       m = m_new;
     }
     const float mc = (m == -INFINITY) ? 0.f : m;
-    // P = p in f16 (V carries vs / rho), stored 16 packed columns (32 keys)
-    // at a time into S buffer j & 1 (P(j-1) V(j-1) reads the other one); the
-    // other copies' columns are zero
+    // P = p in f16 (V carries vs / rho) for this copy's keys, into the P
+    // columns once P(j-1) V(j-1) has read them; the other copies' columns
+    // stay zero
+    constexpr int kChunks = W / 32;  // 32-key chunks of this copy
     float sum[2] = {0.f, 0.f};
+    auto exps = [&](const uint32_t* x, uint32_t* pk) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      constexpr int kChunks = W / 32;  // 32-key chunks of this copy
-      const int owner = q / kChunks;   // copy whose keys fill packed columns [16q, 16q+16)
-      uint32_t pk[16];
-      if (owner == c) {
-        const int h = q % kChunks;
-        uint32_t* x = W <= 64 ? &s[32 * h] : s;
-        if (W > 64) scaled_chunk(h, x);
-#pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float p0 = fast_exp2(__uint_as_float(x[4 * e4]) - mc);
-          const float p1 = fast_exp2(__uint_as_float(x[4 * e4 + 1]) - mc);
-          const float p2 = fast_exp2(__uint_as_float(x[4 * e4 + 2]) - mc);
-          const float p3 = fast_exp2(__uint_as_float(x[4 * e4 + 3]) - mc);
-          sum[0] += p0 + p2;
-          sum[1] += p1 + p3;
-          pk[2 * e4] = pack_f16x2(p0, p1);
-          pk[2 * e4 + 1] = pack_f16x2(p2, p3);
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = 0u;
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const float p0 = fast_exp2(__uint_as_float(x[4 * e4]) - mc);
+        const float p1 = fast_exp2(__uint_as_float(x[4 * e4 + 1]) - mc);
+        const float p2 = fast_exp2(__uint_as_float(x[4 * e4 + 2]) - mc);
+        const float p3 = fast_exp2(__uint_as_float(x[4 * e4 + 3]) - mc);
+        sum[0] += p0 + p2;
+        sum[1] += p1 + p3;
+        pk[2 * e4] = pack_f16x2(p0, p1);
+        pk[2 * e4 + 1] = pack_f16x2(p2, p3);
       }
-      tmem_st16(p_col + 16 * q, pk);
+    };
+    // P(j-1) V(j-1) done: P may be rewritten and O rescaled; waiting every
+    // tile also keeps this barrier's phases in step
+    auto wait_pv = [&]() -> bool {
+      if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE], (uint32_t)(j - 1) & 1u,
+                                                       sh.abort_flag, a.status)))
+        return false;
+      tc_fence_after();
+      return true;
+    };
+    if constexpr (W <= 64) {
+      // the exponentials overlap P(j-1) V(j-1)
+      uint32_t pk[W / 2];
+#pragma unroll
+      for (int h = 0; h < kChunks; ++h) exps(&s[32 * h], &pk[16 * h]);
+      if (!(ok = wait_pv())) break;
+#pragma unroll
+      for (int h = 0; h < kChunks; ++h) tmem_st16(p_base + (col0 >> 1) + 16 * h, &pk[16 * h]);
+    } else {
+      // second pass over S, 32 keys at a time, straight into P
+      if (!(ok = wait_pv())) break;
+#pragma unroll
+      for (int h = 0; h < kChunks; ++h) {
+        uint32_t pk[16];
+        scaled_chunk(h, s);
+        exps(s, pk);
+        tmem_st16(p_base + 16 * h, pk);
+      }
     }
     l += sum[0] + sum[1];
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars[B_K_EMPTY + ks_slot]);  // done with the K tile's scales
-    // O may be rescaled once P(j-1) V(j-1) completed; waiting every tile
-    // also keeps this barrier's phases in step
-    if (j > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE], (uint32_t)(j - 1) & 1u,
-                                             sh.abort_flag, a.status));
-      if (!ok) break;
-    }
-    tc_fence_after();
     if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
@@ -815,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint64_t bd = sdesc_sw128(v0 + kk * 2048, L::kHalfBytes, 1024);
-          umma_bf16_ts(tmem + kColO, tmem + kColS + 128 * (j & 1) + kk * 8, bd, idesc_pv,
+          umma_bf16_ts(tmem + kColO, tmem + kColP + kk * 8, bd, idesc_pv,
                        (j > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&bars[B_O_DONE]);
