@@ -4,8 +4,8 @@
 A step is one pass of the whole path over one iteration's synthetic batch:
 KV append of the iteration's new rows (``mb_kv_append``), planning with the
 one host->device upload of the work lists (``mb_attn_plan``) and the
-attention of every request (``mb_attn_forward``: split-KV / cascade kernel,
-LSE combine, tcgen05 prefill kernel). Inputs are resident in HBM; between
+attention of every request (``mb_attn_forward``: split-KV / cascade kernel
+with the LSE merge of split rows inside it, tcgen05 prefill kernel). Inputs are resident in HBM; between
 timed steps the L2 is flushed by writing a 256 MiB buffer (outside the timed
 events). Each step is timed with CUDA events on the launching stream.
 
@@ -47,9 +47,9 @@ UNIT = "Q rows/s"
 DEFAULT_WORKLOAD = "llama2_7b_orca_iteration"
 PREFILL_MIN_ROWS = 16  # the planner's default split between the two kernels
 FLUSH_BYTES = 256 << 20
-STAGES = ["decode", "combine", "prefill"]
-KERNEL_SOURCES = {"prefill": "prefill.cu", "decode": "decode.cu", "combine": "combine.cu",
-                  "decode_fp8": "decode_fp8.cu"}
+STAGES = ["decode", "prefill"]  # the LSE merge runs inside the split-KV kernels
+STAGE_INDEX = {"decode": 0, "prefill": 2}  # MB_STAGE_DECODE, MB_STAGE_PREFILL
+KERNEL_SOURCES = {"prefill": "prefill.cu", "decode": "decode.cu", "decode_fp8": "decode_fp8.cu"}
 
 
 def parse_args(argv=None):
@@ -462,7 +462,7 @@ def run_gpu(args):
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(STAGES))]
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * B.NUM_STAGES)]
            for _ in range(K)]
     aev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(K)]
@@ -510,9 +510,9 @@ def run_gpu(args):
     torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     stage_ms = {}
-    for si, name in enumerate(STAGES):
-        if info[{"decode": "n_decode_items", "combine": "n_combine",
-                 "prefill": "n_prefill_items"}[name]] > 0:
+    for name in STAGES:
+        si = STAGE_INDEX[name]
+        if info[{"decode": "n_decode_items", "prefill": "n_prefill_items"}[name]] > 0:
             stage_ms[name] = statistics.mean(
                 sev[i][2 * si].elapsed_time(sev[i][2 * si + 1]) for i in range(K))
     stage_ms["append"] = statistics.mean(a.elapsed_time(b) for a, b in aev)

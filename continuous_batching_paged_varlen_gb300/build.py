@@ -19,8 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmb.so")
 SOURCES = ["plan.cpp", "sched.cpp", "api.cu", "kv_append.cu", "rope_append.cu", "decode.cu",
-           "combine.cu", "prefill.cu", "noalloc.cu", "decode_fp8.cu"]
-HEADERS = ["mb_internal.h", "mb_device.cuh", "kernels.h", "plan_impl.h"]
+           "prefill.cu", "noalloc.cu", "decode_fp8.cu"]
+HEADERS = ["mb_internal.h", "mb_device.cuh", "kernels.h", "plan_impl.h", "combine.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I" + os.path.join(ROOT, "include")]

@@ -145,21 +145,18 @@ mb_status_t mb_attn_forward_fp8_timed(const mb_plan_t* plan, const void* q,
     a.lse = lse;
     a.part_o = reinterpret_cast<float*>(ws + d.off_part_o);
     a.part_lse = reinterpret_cast<float*>(ws + d.off_part_lse);
+    a.row_merge = reinterpret_cast<const MergeRef*>(ws + d.off_row_merge);
+    a.combine_count = d.n_combine > 0 ? reinterpret_cast<int32_t*>(ws + d.off_combine_count) : nullptr;
     a.status = reinterpret_cast<int32_t*>(ws);
     rec(MB_STAGE_DECODE, 0);
     e = launch_decode_fp8(a, stream);
     rec(MB_STAGE_DECODE, 1);
     if (e != cudaSuccess) return MB_ERR_CUDA;
   }
-  if (d.n_combine > 0) {
-    rec(MB_STAGE_COMBINE, 0);
-    e = launch_combine(reinterpret_cast<const CombineEntry*>(ws + d.off_combine), d.n_combine,
-                       reinterpret_cast<const float*>(ws + d.off_part_o),
-                       reinterpret_cast<const float*>(ws + d.off_part_lse), d.head_dim,
-                       d.n_q_heads, out, lse, stream, events == nullptr);
-    rec(MB_STAGE_COMBINE, 1);
-    if (e != cudaSuccess) return MB_ERR_CUDA;
-  }
+  // split rows are merged inside the split-KV kernel: the combine stage
+  // is recorded as an empty interval
+  rec(MB_STAGE_COMBINE, 0);
+  rec(MB_STAGE_COMBINE, 1);
   return MB_OK;
 }
 
@@ -300,6 +297,8 @@ mb_status_t mb_attn_forward_timed(const mb_plan_t* plan, const void* q, const vo
     a.lse = lse;
     a.part_o = reinterpret_cast<float*>(ws + d.off_part_o);
     a.part_lse = reinterpret_cast<float*>(ws + d.off_part_lse);
+    a.row_merge = reinterpret_cast<const MergeRef*>(ws + d.off_row_merge);
+    a.combine_count = d.n_combine > 0 ? reinterpret_cast<int32_t*>(ws + d.off_combine_count) : nullptr;
     a.status = status;
     a.k_map = &km;
     a.v_map = &vm;
@@ -308,16 +307,10 @@ mb_status_t mb_attn_forward_timed(const mb_plan_t* plan, const void* q, const vo
     rec(MB_STAGE_DECODE, 1);
     if (e != cudaSuccess) return MB_ERR_CUDA;
   }
-  if (d.n_combine > 0) {
-    rec(MB_STAGE_COMBINE, 0);
-    // overlaps the split-KV kernel's tail (every combine row comes from it)
-    e = launch_combine(reinterpret_cast<const CombineEntry*>(ws + d.off_combine), d.n_combine,
-                       reinterpret_cast<const float*>(ws + d.off_part_o),
-                       reinterpret_cast<const float*>(ws + d.off_part_lse), d.head_dim,
-                       d.n_q_heads, out, lse, stream, events == nullptr);
-    rec(MB_STAGE_COMBINE, 1);
-    if (e != cudaSuccess) return MB_ERR_CUDA;
-  }
+  // split rows are merged inside the split-KV kernel: the combine stage
+  // is recorded as an empty interval
+  rec(MB_STAGE_COMBINE, 0);
+  rec(MB_STAGE_COMBINE, 1);
   return MB_OK;
 }
 

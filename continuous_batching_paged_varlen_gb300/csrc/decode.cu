@@ -13,7 +13,8 @@
 // accumulator; each key is masked by the row's own visibility bound
 // (S0 + i + 1, "How To Scale Your Model notes (7-8)", section 2). The result
 // is the final row (bf16 out + LSE) or, when the key range was split, a
-// normalised partial (fp32 O, log2-domain LSE) for the combine kernel.
+// normalised partial (fp32 O, log2-domain LSE); the CTA that writes a row's
+// last partial merges them all (combine.cuh).
 //
 // This path is bound by HBM bandwidth, so the design spends everything on
 // keeping bytes in flight and almost nothing on issue slots:
@@ -34,6 +35,7 @@
 #include <math.h>
 
 #include "../../include/mb.h"
+#include "combine.cuh"
 #include "kernels.h"
 #include "mb_device.cuh"
 
@@ -97,11 +99,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
 
-  // the combine kernel launched after this one (programmatic stream
-  // serialization) may be scheduled now; it waits for this grid to finish
-  // before it reads the partials
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
   const DecodeItem it = a.items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nr = it.n_rows;
@@ -122,16 +119,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
-  }
-  // gather the item's query rows into the K-major 128-byte-swizzled Q tile
-  // (rows past n_rows are zero)
-  {
+  // Only the barriers are shared before the producer starts: it issues the
+  // first K/V pages while the other warps gather Q and allocate TMEM (a short
+  // step has few tiles, so these latencies would otherwise add up in series).
+  // Its first tile's page ids are loaded before the barrier.
+  const int32_t* btrow = a.block_table + (int64_t)it.bt_row * a.max_blocks;
+  const int last_block = (it.k_end - 1) >> ps_shift;
+  const int first_block = it.k_begin >> ps_shift;  // k_begin is page-aligned
+  int32_t page0 = 0;
+  if (warp == 4 && n > 0 && lane < (BN >> ps_shift))
+    page0 = __ldg(btrow + min(first_block + lane, last_block));
+  __syncthreads();
+  uint32_t tmem = 0;
+  if (warp != 4) {
+    if (warp == 5) {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
+    // gather the item's query rows into the K-major 128-byte-swizzled Q tile
+    // (rows past n_rows are zero): warps 0-3 and 5
     const uint4* q = static_cast<const uint4*>(a.q);
     constexpr int CH = D / 8;  // 16-byte chunks per row
-    for (int idx = threadIdx.x; idx < BM * CH; idx += kThreads) {
+    const int gt = threadIdx.x < 128 ? (int)threadIdx.x : (int)threadIdx.x - 32;
+    for (int idx = gt; idx < BM * CH; idx += kThreads - 32) {
       const int r = idx / CH, c = idx - r * CH;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (r < nr) {
@@ -142,20 +152,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<uint4*>(sq + half * L::kHalfBytes + r * 128 + ((c8 ^ (r & 7)) << 4)) = v;
     }
     fence_proxy_async_smem();
+    tc_fence_before();
+    named_barrier_sync(1, kThreads - 32);
+    tc_fence_after();
+    tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     const int ps = 1 << ps_shift;
     const int npg = BN / ps, nbox = npg * L::kHalves;
     const int my_pg = lane % npg, my_h2 = lane / npg;
-    const int32_t* btrow = a.block_table + (int64_t)it.bt_row * a.max_blocks;
-    const int last_block = (it.k_end - 1) >> ps_shift;
-    const int first_block = it.k_begin >> ps_shift;  // k_begin is page-aligned
     int32_t my_y = 0;
     int issued = 0;
     for (int i = 0; i < 2 * n; ++i) {
@@ -168,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if ((i & 1) == 0 && lane < npg) {
         int b = first_block + j * npg + lane;
         if (b > last_block) b = last_block;  // keys past k_end: masked, V zeroed
-        int32_t page = __ldg(btrow + b);
+        int32_t page = j == 0 ? page0 : __ldg(btrow + b);
         if ((unsigned)page >= (unsigned)a.num_pages) {
           set_status(a.status, MB_ERR_DEVICE_INDEX);
           page = 0;
@@ -389,7 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (valid && final_row && a.lse) a.lse[orow] = lse2 * kLn2;
-      if (valid && !final_row) a.part_lse[rd.dst] = lse2;
+      if (valid && !final_row) {
+        a.part_lse[rd.dst] = lse2;
+        __threadfence();  // the partial is visible before this CTA counts it
+      }
     }
   }
 
@@ -398,6 +408,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  if (a.combine_count) {
+    dev::MergeArgs mg;
+    mg.rows = a.rows + it.row_begin;
+    mg.refs = a.row_merge + it.row_begin;
+    mg.n_rows = nr;
+    mg.count = a.combine_count;
+    mg.part_o = a.part_o;
+    mg.part_lse = a.part_lse;
+    mg.n_q_heads = a.n_q_heads;
+    mg.out = static_cast<__nv_bfloat16*>(a.out);
+    mg.lse = a.lse;
+    // the Q tile is no longer read (every MMA has completed)
+    dev::merge_completed_rows<D, kThreads>(mg, reinterpret_cast<uint32_t*>(sq));
   }
 }
 

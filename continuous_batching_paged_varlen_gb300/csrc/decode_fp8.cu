@@ -7,7 +7,8 @@
 // bf16 split-KV kernel runs (one CTA = up to 128 query rows of one KV head
 // against the key range [k_begin, k_end) of one block-table row, "How To
 // Scale Your Model notes (7-8)", section 3), and the results are the same
-// final rows or normalised partials for the combine kernel.
+// final rows or normalised partials, merged by the CTA that completes a row
+// (combine.cuh).
 //
 // The scales of key j factor out of both products:
 //   S[r][j] = ks_j sq_r (qc_r . kcode_j)    O[r] = rho sum_j p[r][j] (vs_j / rho) vcode_j
@@ -51,6 +52,7 @@
 #include <math.h>
 
 #include "../../include/mb.h"
+#include "combine.cuh"
 #include "kernels.h"
 #include "mb_device.cuh"
 
@@ -477,7 +479,10 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
       }
     }
     if (valid && final_row && a.lse) a.lse[orow] = lse2 * 0.6931471805599453f;
-    if (valid && !final_row) a.part_lse[rd.dst] = lse2;
+    if (valid && !final_row) {
+      a.part_lse[rd.dst] = lse2;
+      __threadfence();  // the partial is visible before this CTA counts it
+    }
   } else {
     // merge the R copies (split-KV partitions of the row's keys): every warp
     // parks its lanes' m, l and O, then finishes D / R columns of its row
@@ -546,6 +551,7 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
         if (final_row && a.lse) a.lse[orow] = lse2 * 0.6931471805599453f;
         if (!final_row) a.part_lse[rd.dst] = lse2;
       }
+      if (!final_row) __threadfence();  // each copy's columns are visible before the count
     }
   }
 }
@@ -566,16 +572,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
 
-  // the combine kernel launched after this one may be scheduled now; it
-  // waits for this grid to finish before it reads the partials
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
   const DecodeItem it = a.items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nr = it.n_rows;
   const int n = ceil_div(it.k_end - it.k_begin, BN);
   const int nw = ceil_div(nr, 32);
   const int ngrp = nw <= 1 ? 1 : (nw == 2 ? 2 : 4);  // row groups; 4 / ngrp copies per row
+  // the producer's first block-table entries load while the CTA sets up
+  int32_t page0 = 0;
+  if (warp == 8 && n > 0 && lane < (BN >> ps_shift))
+    page0 = __ldg(a.block_table + (int64_t)it.bt_row * a.max_blocks +
+                  min((it.k_begin >> ps_shift) + lane, (it.k_end - 1) >> ps_shift));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < L::kKSlots; ++s) {
@@ -633,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return ((int64_t)page * a.n_kv_heads + it.kv_head) << ps_shift;
     };
-    int32_t next_page = lane < npg ? page_of(0) : 0;
+    int32_t next_page = lane < npg ? page0 : 0;
     int64_t cur_row = 0, prev_row = 0;  // tiles of the latest and the previous K item
     int nk = 0, nv = 0;                 // K / V tiles issued
     for (int s = 0; s < 2 * n; ++s) {
@@ -869,6 +876,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  if (a.combine_count) {
+    dev::MergeArgs mg;
+    mg.rows = a.rows + it.row_begin;
+    mg.refs = a.row_merge + it.row_begin;
+    mg.n_rows = nr;
+    mg.count = a.combine_count;
+    mg.part_o = a.part_o;
+    mg.part_lse = a.part_lse;
+    mg.n_q_heads = a.n_q_heads;
+    mg.out = static_cast<__nv_bfloat16*>(a.out);
+    mg.lse = a.lse;
+    // the K ring is no longer written (every copy has landed) nor read
+    dev::merge_completed_rows<D, kThreads>(mg, reinterpret_cast<uint32_t*>(sk));
   }
 }
 

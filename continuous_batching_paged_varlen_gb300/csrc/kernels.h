@@ -44,6 +44,11 @@ struct DecodeArgs {
   float* lse;        // nullable
   float* part_o;
   float* part_lse;   // log2 domain
+  // split rows: per row its merge reference, and one arrival counter per
+  // combine entry (zero between launches); the CTA completing a row merges
+  // it (combine.cuh). combine_count null: no split rows.
+  const MergeRef* row_merge;
+  int32_t* combine_count;
   int32_t* status;
   const CUtensorMap* k_map;  // host copies, passed by value to the kernel
   const CUtensorMap* v_map;
@@ -71,18 +76,12 @@ struct DecodeFp8Args {
   float* lse;
   float* part_o;
   float* part_lse;
+  const MergeRef* row_merge;  // as in DecodeArgs
+  int32_t* combine_count;
   int32_t* status;
   const CUtensorMap* k_map;  // uint8 codes [rows, D], box D x ps, swizzled (host copy)
 };
 cudaError_t launch_decode_fp8(const DecodeFp8Args& a, cudaStream_t s);
-
-// LSE merge of partials (combine.cu). overlap_previous: launch with
-// programmatic stream serialization after the split-KV kernel (the combine
-// kernel waits for that grid's completion before reading partials).
-cudaError_t launch_combine(const CombineEntry* entries, int32_t n, const float* part_o,
-                           const float* part_lse, int32_t head_dim, int32_t n_q_heads,
-                           void* out, float* lse, cudaStream_t s,
-                           bool overlap_previous = false);
 
 // tcgen05 prefill kernel (prefill.cu).
 struct PrefillArgs {

@@ -64,7 +64,17 @@ struct CombineEntry {
   int32_t n_slots;
 };
 
+// Per decode row (parallel to the RowDesc array): where a split row's
+// partials live and which arrival counter completes it.
+struct MergeRef {
+  int32_t entry;       // combine entry of the row; -1: the row is final
+  int32_t n_slots;     // partials of the output row
+  int32_t slot_begin;  // its first partial slot
+  int32_t pad;
+};
+
 static_assert(sizeof(DecodeItem) == 32, "layout");
+static_assert(sizeof(MergeRef) == 16, "layout");
 static_assert(sizeof(RowDesc) == 16, "layout");
 static_assert(sizeof(PrefillItem) == 32, "layout");
 static_assert(sizeof(CombineEntry) == 16, "layout");
@@ -75,8 +85,8 @@ struct PlanDevice {
   int32_t n_q_heads, n_kv_heads, head_dim, page_size, num_pages, max_blocks;
   int32_t total_q;
   float scale;
-  size_t off_decode_items, off_rows, off_prefill_items, off_combine, off_part_lse,
-      off_part_o;
+  size_t off_decode_items, off_rows, off_prefill_items, off_combine, off_row_merge,
+      off_combine_count, off_part_lse, off_part_o;
   size_t metadata_bytes, workspace_bytes;
 };
 

@@ -138,17 +138,13 @@ extern "C" mb_status_t mb_attn_forward_noalloc(const mb_plan_t* plan, const void
     a.lse = lse;
     a.part_o = reinterpret_cast<float*>(ws + d.off_part_o);
     a.part_lse = reinterpret_cast<float*>(ws + d.off_part_lse);
+    a.row_merge = reinterpret_cast<const MergeRef*>(ws + d.off_row_merge);
+    a.combine_count = d.n_combine > 0 ? reinterpret_cast<int32_t*>(ws + d.off_combine_count) : nullptr;
     a.status = status;
     a.k_map = &km;
     a.v_map = &vm;
     if (launch_decode(a, stream) != cudaSuccess) return MB_ERR_CUDA;
   }
-  if (d.n_combine > 0 &&
-      launch_combine(reinterpret_cast<const CombineEntry*>(ws + d.off_combine), d.n_combine,
-                     reinterpret_cast<const float*>(ws + d.off_part_o),
-                     reinterpret_cast<const float*>(ws + d.off_part_lse), d.head_dim,
-                     d.n_q_heads, out, lse, stream) != cudaSuccess)
-    return MB_ERR_CUDA;
   if (d.n_prefill_items > 0) {
     CUtensorMap qm;
     const cuuint64_t qdims[3] = {(cuuint64_t)d.head_dim, (cuuint64_t)d.n_q_heads,

@@ -452,6 +452,13 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
   off = align256(off + pitems.size() * sizeof(PrefillItem));
   d.off_combine = off;
   off = align256(off + combine.size() * sizeof(CombineEntry));
+  // per decode row its merge reference, then one arrival counter per entry
+  // (zero in the image; the split-KV kernel puts each back to zero after
+  // its merge)
+  d.off_row_merge = off;
+  off = align256(off + rows.size() * sizeof(MergeRef));
+  d.off_combine_count = off;
+  off = align256(off + combine.size() * sizeof(int32_t));
   d.metadata_bytes = off;
   d.off_part_lse = off;
   off = align256(off + (size_t)n_partials * sizeof(float));
@@ -468,6 +475,23 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
     memcpy(img + d.off_prefill_items, pitems.data(), pitems.size() * sizeof(PrefillItem));
   if (!combine.empty())
     memcpy(img + d.off_combine, combine.data(), combine.size() * sizeof(CombineEntry));
+  {
+    std::vector<int32_t> slot_entry((size_t)n_partials, -1);
+    for (size_t e = 0; e < combine.size(); ++e)
+      for (int32_t k = 0; k < combine[e].n_slots; ++k)
+        slot_entry[(size_t)combine[e].slot_begin + k] = (int32_t)e;
+    MergeRef* mr = reinterpret_cast<MergeRef*>(img + d.off_row_merge);
+    for (size_t i = 0; i < rows.size(); ++i) {
+      MergeRef ref = {-1, 0, 0, 0};
+      if (rows[i].dst >= 0) {
+        const CombineEntry& ce = combine[(size_t)slot_entry[(size_t)rows[i].dst]];
+        ref.entry = slot_entry[(size_t)rows[i].dst];
+        ref.n_slots = ce.n_slots;
+        ref.slot_begin = ce.slot_begin;
+      }
+      mr[i] = ref;
+    }
+  }
 
   mb_plan_info_t& info = plan->info;
   info = mb_plan_info_t{};
@@ -480,7 +504,7 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
   info.cascade_keys = cascade_keys;
   info.kv_chunk = chunk;
   info.total_q = total_q;
-  info.n_launches = (d.n_decode_items > 0) + (d.n_prefill_items > 0) + (d.n_combine > 0);
+  info.n_launches = (d.n_decode_items > 0) + (d.n_prefill_items > 0);
   info.workspace_bytes = d.workspace_bytes;
   info.metadata_bytes = d.metadata_bytes;
   return MB_OK;

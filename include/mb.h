@@ -111,7 +111,7 @@ typedef struct {
   int32_t n_decode_items;    /* CTAs of the split-KV kernel                   */
   int32_t n_decode_rows;     /* row descriptors                               */
   int32_t n_prefill_items;   /* CTAs of the prefill kernel                    */
-  int32_t n_combine;         /* output rows merged by the combine kernel      */
+  int32_t n_combine;         /* output rows merged from split-KV partials     */
   int32_t n_partials;        /* partial (O, LSE) slots                        */
   int32_t n_cascade_groups;  /* shared-prefix groups                          */
   int32_t cascade_keys;      /* keys read once per group (sum over groups)    */

@@ -290,3 +290,29 @@ def test_fp8_matches_bf16_path_closely():
     np.testing.assert_allclose(out8.float().cpu().numpy(), out.float().cpu().numpy(),
                                rtol=TOL, atol=TOL)
     assert math.isfinite(float(lse8.sum()))
+
+
+def test_fp8_split_rows_merged_on_every_forward():
+    """The fused merge's arrival counters return to zero after each forward:
+    one plan run three times gives the same complete rows."""
+    shapes, hq, hkv, d, ps, shared = CASES["shared_prefix"]
+    w = custom_workload(shapes, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, page_size=ps,
+                        seed=31, shared_prefix=shared)
+    k8, v8, ks, vs, cfg = fill_fp8(w)
+    plan = B.Plan(w.requests, w.block_table, cfg, opts=B.options(**SPLIT_KV_ONLY, kv_chunk=64))
+    assert plan.info.n_combine > 0
+    bt = torch.from_numpy(np.ascontiguousarray(w.block_table)).cuda()
+    q = w.q.cuda()
+    res = []
+    for _ in range(3):
+        out = torch.full((w.total_q, hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((w.total_q, hq), float("nan"), dtype=torch.float32, device="cuda")
+        plan.forward_fp8(q, k8, v8, ks, vs, bt, out, lse)
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        res.append((out, lse))
+    plan.close()
+    for out, lse in res[1:]:
+        assert torch.equal(out.view(torch.int16), res[0][0].view(torch.int16))
+        assert torch.equal(lse.view(torch.int32), res[0][1].view(torch.int32))
+    check_all(w, *res[0])

@@ -210,3 +210,43 @@ def test_deterministic_and_empty():
     assert plan.info.n_launches == 0
     plan.forward(None, None, None, None, None)
     plan.close()
+
+
+@pytest.mark.parametrize("name,opts", [("tiny_mixed", dict(kv_chunk=64)),
+                                       ("shared_prefix_decode", {}),
+                                       ("spec_decode_k3", dict(kv_chunk=256))])
+def test_split_rows_merged_on_every_forward(name, opts):
+    """Split rows are merged by the CTA that completes them, through per-row
+    arrival counters that each merge puts back to zero: the same plan run
+    again (and again) must give the same, complete rows."""
+    if name == "spec_decode_k3":  # a bounded share of the batch
+        sp = W.SPECS[name]
+        w = custom_workload(W.request_shapes(sp)[:24], n_q_heads=sp.n_q_heads,
+                            n_kv_heads=sp.n_kv_heads, head_dim=sp.head_dim,
+                            page_size=sp.page_size, seed=5)
+    else:
+        w = W.make_workload(name)
+    kc, vc, cfg = fill_cache(w)
+    plan = B.Plan(w.requests, w.block_table, cfg, opts=B.options(**opts))
+    assert plan.info.n_combine > 0 and plan.info.n_launches == 1 + (plan.info.n_prefill_items > 0)
+    s = w.spec
+    q = w.q.cuda()
+    bt = torch.from_numpy(np.ascontiguousarray(w.block_table)).cuda()
+    results = []
+    for _ in range(3):
+        out = torch.full((w.total_q, s.n_q_heads, s.head_dim), float("nan"), dtype=torch.bfloat16,
+                         device="cuda")
+        lse = torch.full((w.total_q, s.n_q_heads), float("nan"), dtype=torch.float32,
+                         device="cuda")
+        plan.forward(q, kc, vc, bt, out, lse)
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        results.append((out, lse))
+    plan.close()
+    for out, lse in results[1:]:
+        assert torch.equal(out.view(torch.int16), results[0][0].view(torch.int16))
+        assert torch.equal(lse.view(torch.int32), results[0][1].view(torch.int32))
+    out, lse = results[0]
+    for r in range(w.n_requests):
+        if w.requests[r, 1] > w.requests[r, 0]:
+            assert_request_close(w, out, lse, r, heads=range(0, s.n_q_heads, 7))
