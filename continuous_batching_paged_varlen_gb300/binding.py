@@ -21,6 +21,7 @@ MB_OK = 0
 STATUS_NAMES = {0: "MB_OK", 1: "MB_ERR_INVALID_ARG", 2: "MB_ERR_SHAPE",
                 3: "MB_ERR_UNSUPPORTED", 4: "MB_ERR_WORKSPACE", 5: "MB_ERR_CUDA",
                 6: "MB_ERR_TIMEOUT", 7: "MB_ERR_DEVICE_INDEX"}
+MB_ERR_WORKSPACE = 4
 MB_ERR_TIMEOUT = 6
 MB_ERR_DEVICE_INDEX = 7
 STAGE_DECODE, STAGE_COMBINE, STAGE_PREFILL, NUM_STAGES = 0, 1, 2, 3
@@ -315,24 +316,32 @@ class Plan:
         self.bt = _host_i32(block_table)
         self.cfg = cfg
         L = lib()
-        nbytes = ctypes.c_size_t(0)
-        check(L.mb_attn_plan_ex(self.reqs.ctypes.data, self.reqs.shape[0], self.bt.ctypes.data,
-                                ctypes.byref(cfg), ctypes.byref(opts) if opts else None, None,
-                                ctypes.byref(nbytes), None, None),
-              "mb_attn_plan (size query)")
-        self.workspace_bytes = int(nbytes.value)
-        if workspace is None or workspace.numel() < self.workspace_bytes:
-            workspace = torch.empty(max(self.workspace_bytes, 256), dtype=torch.uint8,
-                                    device=device)
-        self.workspace = workspace
+        o = ctypes.byref(opts) if opts else None
         h = ctypes.c_void_p()
-        nb = ctypes.c_size_t(workspace.numel())
-        check(L.mb_attn_plan_ex(self.reqs.ctypes.data, self.reqs.shape[0], self.bt.ctypes.data,
-                                ctypes.byref(cfg), ctypes.byref(opts) if opts else None,
-                                _ptr(workspace), ctypes.byref(nb), _stream_ptr(stream),
-                                ctypes.byref(h)),
-              "mb_attn_plan")
+        st = MB_ERR_WORKSPACE
+        if workspace is not None:
+            # a caller's workspace is tried first: a plan that fits needs no
+            # size query (the planner runs once)
+            nb = ctypes.c_size_t(workspace.numel())
+            st = L.mb_attn_plan_ex(self.reqs.ctypes.data, self.reqs.shape[0],
+                                   self.bt.ctypes.data, ctypes.byref(cfg), o, _ptr(workspace),
+                                   ctypes.byref(nb), _stream_ptr(stream), ctypes.byref(h))
+        if st == MB_ERR_WORKSPACE:
+            nbytes = ctypes.c_size_t(0)
+            check(L.mb_attn_plan_ex(self.reqs.ctypes.data, self.reqs.shape[0],
+                                    self.bt.ctypes.data, ctypes.byref(cfg), o, None,
+                                    ctypes.byref(nbytes), None, None),
+                  "mb_attn_plan (size query)")
+            workspace = torch.empty(max(int(nbytes.value), 256), dtype=torch.uint8,
+                                    device=device)
+            nb = ctypes.c_size_t(workspace.numel())
+            st = L.mb_attn_plan_ex(self.reqs.ctypes.data, self.reqs.shape[0],
+                                   self.bt.ctypes.data, ctypes.byref(cfg), o, _ptr(workspace),
+                                   ctypes.byref(nb), _stream_ptr(stream), ctypes.byref(h))
+        check(st, "mb_attn_plan")
+        self.workspace = workspace
         self._h = h
+        self.workspace_bytes = int(self.info.workspace_bytes)
 
     @property
     def info(self) -> PlanInfo:

@@ -39,44 +39,35 @@ struct MergeArgs {
   float* lse;                    // nullable, natural log
 };
 
-// Called by all kThreads threads of the CTA after a __syncthreads that
-// follows every partial write (and its __threadfence) of this CTA.
-// scratch: >= 4 * 129 words of shared memory nobody else uses any more.
+// One arrival on a split row's counter, by a thread whose partial (or
+// share of one) is already fenced. `add` of `total` arrivals completes the
+// row; the completing thread gets true and puts the counter back to zero
+// (every other arrival of this launch is in), so the next launch starts
+// clean.
+__device__ __forceinline__ bool arrive_partial(int32_t* count, int add, int total) {
+  if (atomicAdd(count, add) + add != total) return false;
+  *count = 0;
+  return true;
+}
+
+// Merge the listed rows (x: flat output row q_index * Hq + q_head, y: first
+// partial slot, z: partials): all kThreads threads of the CTA, one per
+// (row, 4 head dims); every thread of a row derives the same max and sum
+// from the row's LSEs; slots in groups of 16 whose loads are all in flight
+// together, rescaled online between groups. The caller fences between the
+// arrivals it observed and this call; partials are read through L2.
 template <int D, int kThreads>
-__device__ __forceinline__ void merge_completed_rows(const MergeArgs& m, uint32_t* scratch) {
+__device__ __forceinline__ void merge_listed_rows(const int4* list, int nl, const float* part_o,
+                                                  const float* part_lse, __nv_bfloat16* out,
+                                                  float* lse) {
   static_assert(D % 4 == 0, "head dim");
-  int* count_n = reinterpret_cast<int*>(scratch + 4 * 128);
-  int4* list = reinterpret_cast<int4*>(scratch);  // [128] (out row, slot_begin, n_slots, -)
-  const int tid = threadIdx.x;
-  if (tid == 0) *count_n = 0;
-  __syncthreads();
-  if (tid < m.n_rows) {
-    const MergeRef ref = m.refs[tid];
-    if (ref.entry >= 0) {
-      const RowDesc rd = m.rows[tid];
-      if (atomicAdd(&m.count[ref.entry], 1) == ref.n_slots - 1) {
-        m.count[ref.entry] = 0;  // every arrival of this launch is in: reset for the next
-        list[atomicAdd(count_n, 1)] =
-            make_int4(rd.q_index * m.n_q_heads + rd.q_head, ref.slot_begin, ref.n_slots, 0);
-      }
-    }
-  }
-  __syncthreads();
-  const int nl = *count_n;
-  if (nl == 0) return;
-  // the other CTAs fenced their partials before arriving: order this CTA's
-  // reads after the arrivals it observed (and read through L2 below)
-  __threadfence();
-  // one thread per (row, 4 head dims): every thread of a row derives the same
-  // max and sum from the row's LSEs; slots in groups of 16 whose loads are
-  // all in flight together, rescaled online between groups
   constexpr int Q4 = D / 4;
   constexpr int G = 16;
-  for (int task = tid; task < nl * Q4; task += kThreads) {
+  for (int task = threadIdx.x; task < nl * Q4; task += kThreads) {
     const int i = task / Q4, q4 = task - i * Q4;
     const int4 e = list[i];
-    const float* lp = m.part_lse + e.y;
-    const float4* op = reinterpret_cast<const float4*>(m.part_o + (int64_t)e.y * D) + q4;
+    const float* lp = part_lse + e.y;
+    const float4* op = reinterpret_cast<const float4*>(part_o + (int64_t)e.y * D) + q4;
     float M = -INFINITY, L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < e.z; s0 += G) {
@@ -114,9 +105,38 @@ __device__ __forceinline__ void merge_completed_rows(const MergeArgs& m, uint32_
     uint2 pk;
     pk.x = pack_bf16x2(acc.x * il, acc.y * il);
     pk.y = pack_bf16x2(acc.z * il, acc.w * il);
-    *reinterpret_cast<uint2*>(m.out + (int64_t)e.x * D + 4 * q4) = pk;
-    if (q4 == 0 && m.lse) m.lse[e.x] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+    *reinterpret_cast<uint2*>(out + (int64_t)e.x * D + 4 * q4) = pk;
+    if (q4 == 0 && lse) lse[e.x] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
   }
+}
+
+// The whole step for a kernel whose rows' partials may have several writer
+// threads: called by all kThreads threads after a __syncthreads that follows
+// every partial write (and its __threadfence) of this CTA; thread r counts
+// row r. scratch: >= 4 * 129 words of shared memory nobody else uses.
+template <int D, int kThreads>
+__device__ __forceinline__ void merge_completed_rows(const MergeArgs& m, uint32_t* scratch) {
+  int* count_n = reinterpret_cast<int*>(scratch + 4 * 128);
+  int4* list = reinterpret_cast<int4*>(scratch);
+  const int tid = threadIdx.x;
+  if (tid == 0) *count_n = 0;
+  __syncthreads();
+  if (tid < m.n_rows) {
+    const MergeRef ref = m.refs[tid];
+    if (ref.entry >= 0) {
+      const RowDesc rd = m.rows[tid];
+      if (arrive_partial(m.count + ref.entry, 1, ref.n_slots))
+        list[atomicAdd(count_n, 1)] =
+            make_int4(rd.q_index * m.n_q_heads + rd.q_head, ref.slot_begin, ref.n_slots, 0);
+    }
+  }
+  __syncthreads();
+  const int nl = *count_n;
+  if (nl == 0) return;
+  // the other CTAs fenced their partials before arriving: order this CTA's
+  // reads after the arrivals it observed
+  __threadfence();
+  merge_listed_rows<D, kThreads>(list, nl, m.part_o, m.part_lse, m.out, m.lse);
 }
 
 }  // namespace dev

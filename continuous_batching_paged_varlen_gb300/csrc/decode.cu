@@ -98,6 +98,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
+  // split rows this CTA completed, to merge before it exits: the count in
+  // the misc words, the list over the Q tile (no longer read by then)
+  int* merge_n = reinterpret_cast<int*>(smem + L::misc_off + 8);
+  int4* merge_list = reinterpret_cast<int4*>(sq);
 
   const DecodeItem it = a.items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -117,12 +121,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[B_O_DONE], 1);
     mbar_init(&bars[B_VZ_READY], 1);
     *abort_flag = 0;
+    *merge_n = 0;
     fence_barrier_init();
   }
-  // Only the barriers are shared before the producer starts: it issues the
-  // first K/V pages while the other warps gather Q and allocate TMEM (a short
-  // step has few tiles, so these latencies would otherwise add up in series).
-  // Its first tile's page ids are loaded before the barrier.
+  // Only the barriers are shared before the producer starts (a short step
+  // has few tiles, so setup latencies would otherwise add up in series): it
+  // issues K_0 at once, then waits until the other warps have issued their
+  // Q loads, so that those enter the memory system ahead of the rest of the
+  // ring (behind ~200 KB of copies per SM, a dependent gather waits
+  // microseconds). Its first tile's page ids are loaded before the barrier.
   const int32_t* btrow = a.block_table + (int64_t)it.bt_row * a.max_blocks;
   const int last_block = (it.k_end - 1) >> ps_shift;
   const int first_block = it.k_begin >> ps_shift;  // k_begin is page-aligned
@@ -137,19 +144,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_relinquish();
     }
     // gather the item's query rows into the K-major 128-byte-swizzled Q tile
-    // (rows past n_rows are zero): warps 0-3 and 5
+    // (rows past n_rows are zero): warps 0-3 and 5, every load in flight
+    // before the producer is released, then the stores
     const uint4* q = static_cast<const uint4*>(a.q);
     constexpr int CH = D / 8;  // 16-byte chunks per row
+    constexpr int kGather = kThreads - 32;
+    constexpr int kPer = (BM * CH + kGather - 1) / kGather;
     const int gt = threadIdx.x < 128 ? (int)threadIdx.x : (int)threadIdx.x - 32;
-    for (int idx = gt; idx < BM * CH; idx += kThreads - 32) {
+    uint4 qv[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int idx = gt + k * kGather;
       const int r = idx / CH, c = idx - r * CH;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (r < nr) {
+      qv[k] = make_uint4(0u, 0u, 0u, 0u);
+      if (idx < BM * CH && r < nr) {
         const RowDesc rd = a.rows[it.row_begin + r];
-        v = __ldg(q + ((int64_t)rd.q_index * a.n_q_heads + rd.q_head) * CH + c);
+        qv[k] = __ldg(q + ((int64_t)rd.q_index * a.n_q_heads + rd.q_head) * CH + c);
       }
+    }
+    named_barrier_arrive(2, kThreads);  // the producer's wait below
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int idx = gt + k * kGather;
+      const int r = idx / CH, c = idx - r * CH;
       const int half = c >> 3, c8 = c & 7;
-      *reinterpret_cast<uint4*>(sq + half * L::kHalfBytes + r * 128 + ((c8 ^ (r & 7)) << 4)) = v;
+      if (idx < BM * CH)
+        *reinterpret_cast<uint4*>(sq + half * L::kHalfBytes + r * 128 + ((c8 ^ (r & 7)) << 4)) =
+            qv[k];
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -168,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2 * n; ++i) {
       const int j = i >> 1, slot = i % kSlots;
       const uint32_t ph = (uint32_t)(i / kSlots) & 1u;
+      if (i == 1) named_barrier_sync(2, kThreads);  // every Q load issued (n >= 1)
       if (i >= kSlots &&
           !__all_sync(0xffffffffu, mbar_wait(&bars[B_KV_EMPTY + slot], ph ^ 1u, abort_flag,
                                              a.status)))
@@ -277,6 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     rd.vis_end = 0;
     rd.dst = -1;
     if (valid) rd = a.rows[it.row_begin + r];
+    MergeRef ref = {-1, 0, 0, 0};
+    if (valid && rd.dst >= 0) ref = a.row_merge[it.row_begin + r];
     // visible keys of this row inside the item: [k_begin, min(k_end, vis_end))
     const int vis_hi = min(it.k_end, rd.vis_end);
     const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
@@ -396,10 +420,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (valid && final_row && a.lse) a.lse[orow] = lse2 * kLn2;
-      if (valid && !final_row) {
-        a.part_lse[rd.dst] = lse2;
-        __threadfence();  // the partial is visible before this CTA counts it
-      }
+      if (valid && !final_row) a.part_lse[rd.dst] = lse2;
+    }
+    // one arrival per partial row, also after an abort (the counters must
+    // stay in step for the next launch); the partial is fenced before it
+    if (valid && rd.dst >= 0) {
+      __threadfence();
+      if (dev::arrive_partial(a.combine_count + ref.entry, 1, ref.n_slots))
+        merge_list[atomicAdd(merge_n, 1)] =
+            make_int4(rd.q_index * a.n_q_heads + rd.q_head, ref.slot_begin, ref.n_slots, 0);
     }
   }
 
@@ -409,19 +438,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (a.combine_count) {
-    dev::MergeArgs mg;
-    mg.rows = a.rows + it.row_begin;
-    mg.refs = a.row_merge + it.row_begin;
-    mg.n_rows = nr;
-    mg.count = a.combine_count;
-    mg.part_o = a.part_o;
-    mg.part_lse = a.part_lse;
-    mg.n_q_heads = a.n_q_heads;
-    mg.out = static_cast<__nv_bfloat16*>(a.out);
-    mg.lse = a.lse;
-    // the Q tile is no longer read (every MMA has completed)
-    dev::merge_completed_rows<D, kThreads>(mg, reinterpret_cast<uint32_t*>(sq));
+  const int nl = *reinterpret_cast<volatile int*>(merge_n);
+  if (nl > 0) {
+    // the other CTAs fenced their partials before arriving: order this
+    // CTA's reads after the arrivals it observed
+    __threadfence();
+    dev::merge_listed_rows<D, kThreads>(merge_list, nl, a.part_o, a.part_lse,
+                                        static_cast<__nv_bfloat16*>(a.out), a.lse);
   }
 }
 
@@ -439,17 +462,22 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, bool overlap_prev
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap_previous ? 1 : 0;
+  static OncePerDevice setup128, setup64;
   cudaError_t e;
   if (a.head_dim == 128) {
     cfg.dynamicSmemBytes = Layout<128>::kAlloc;
-    e = cudaFuncSetAttribute(splitkv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)Layout<128>::kAlloc);
+    e = setup128.run([](int) {
+      return cudaFuncSetAttribute(splitkv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)Layout<128>::kAlloc);
+    });
     if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, splitkv_kernel<128>, a, ps_shift, *a.k_map, *a.v_map);
   }
   cfg.dynamicSmemBytes = Layout<64>::kAlloc;
-  e = cudaFuncSetAttribute(splitkv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)Layout<64>::kAlloc);
+  e = setup64.run([](int) {
+    return cudaFuncSetAttribute(splitkv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Layout<64>::kAlloc);
+  });
   if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, splitkv_kernel<64>, a, ps_shift, *a.k_map, *a.v_map);
 }

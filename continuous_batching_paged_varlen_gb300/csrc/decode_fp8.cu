@@ -255,21 +255,24 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
   const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
 
   // this lane's query row as sq * (hi + lo), the hi / lo codes into TMEM
-  // (the A operands of Q K^T); lanes without a row hold zeros
+  // (the A operands of Q K^T); lanes without a row hold zeros. The row's
+  // loads are all issued before the producer is let past its first tile,
+  // so they reach memory ahead of the rest of the ring.
   float sq = 0.f;
   {
     const uint4* qrow = static_cast<const uint4*>(a.q) +
                         ((int64_t)rd.q_index * a.n_q_heads + rd.q_head) * (D / 8);
-    float amax = 0.f;
-    if (valid) {
-#pragma unroll 4
-      for (int k = 0; k < D / 8; ++k) {
-        const uint4 b = __ldg(qrow + k);
-        const uint32_t wv[4] = {b.x, b.y, b.z, b.w};
+    uint4 qb[D / 8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          amax = fmax3(amax, fabsf(bf16_lo(wv[e])), fabsf(bf16_hi(wv[e])));
-      }
+    for (int k = 0; k < D / 8; ++k) qb[k] = valid ? __ldg(qrow + k) : make_uint4(0u, 0u, 0u, 0u);
+    named_barrier_arrive(2, 160);  // the producer's wait
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < D / 8; ++k) {
+      const uint32_t wv[4] = {qb[k].x, qb[k].y, qb[k].z, qb[k].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        amax = fmax3(amax, fabsf(bf16_lo(wv[e])), fabsf(bf16_hi(wv[e])));
     }
     sq = amax * (1.f / 448.f);
     const float inv = amax > 0.f ? 448.f / amax : 0.f;
@@ -280,7 +283,7 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
       uint32_t hi[QH], lo[QH];
 #pragma unroll
       for (int k = 0; k < QH / 2; ++k) {  // one 16-byte chunk = 8 values = 2 columns
-        uint4 b = make_uint4(0u, 0u, 0u, 0u);
+        uint4 b = make_uint4(0u, 0u, 0u, 0u);  // the row again, from L1
         if (valid) b = __ldg(qrow + hh * (QH / 2) + k);
         split4(bf16_lo(b.x) * inv, bf16_hi(b.x) * inv, bf16_lo(b.y) * inv, bf16_hi(b.y) * inv,
                hi[2 * k], lo[2 * k]);
@@ -644,6 +647,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t cur_row = 0, prev_row = 0;  // tiles of the latest and the previous K item
     int nk = 0, nv = 0;                 // K / V tiles issued
     for (int s = 0; s < 2 * n; ++s) {
+      // after the first K tile: wait until the softmax warps have issued
+      // their Q loads (2 n >= 2, and no wait before this one can fail)
+      if (s == 1) named_barrier_sync(2, 160);
       const SeqItem si = seq_item(s, n);
       const int j = si.j;
       const int slot = si.v ? j % L::kVStSlots : j % L::kKSlots;
@@ -898,18 +904,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_decode_fp8(const DecodeFp8Args& a, cudaStream_t s) {
   if (a.n_items <= 0) return cudaSuccess;
   const int ps_shift = __builtin_ctz((unsigned)a.page_size);
+  static OncePerDevice setup128, setup64;
   cudaError_t e;
   if (a.head_dim == 128) {
-    e = cudaFuncSetAttribute(splitkv_fp8_kernel<128>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)Layout<128>::kAlloc);
+    e = setup128.run([](int) {
+      return cudaFuncSetAttribute(splitkv_fp8_kernel<128>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)Layout<128>::kAlloc);
+    });
     if (e != cudaSuccess) return e;
     splitkv_fp8_kernel<128><<<(unsigned)a.n_items, kThreads, Layout<128>::kAlloc, s>>>(
         a, ps_shift, *a.k_map);
     return cudaGetLastError();
   }
-  e = cudaFuncSetAttribute(splitkv_fp8_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)Layout<64>::kAlloc);
+  e = setup64.run([](int) {
+    return cudaFuncSetAttribute(splitkv_fp8_kernel<64>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Layout<64>::kAlloc);
+  });
   if (e != cudaSuccess) return e;
   splitkv_fp8_kernel<64><<<(unsigned)a.n_items, kThreads, Layout<64>::kAlloc, s>>>(
       a, ps_shift, *a.k_map);

@@ -5,9 +5,29 @@
 #include <cuda_runtime_api.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "mb_internal.h"
 
 namespace mb {
+
+// Launch attributes a kernel needs once per device (its dynamic shared
+// memory size, a device property): `setup` runs on the first launch on each
+// of the first 64 devices, and on every launch beyond them.
+struct OncePerDevice {
+  std::atomic<uint64_t> done{0};
+  template <class F>
+  cudaError_t run(F&& setup) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = setup(dev);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+  }
+};
 
 // KV append scatter (kv_append.cu).
 cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new,

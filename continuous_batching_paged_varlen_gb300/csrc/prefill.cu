@@ -603,21 +603,35 @@ cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
   p.lse = a.lse;
   p.status = a.status;
   constexpr uint32_t smem = Layout<D>::kAlloc;
-  // the register split assumes the kernel launches with kLaunchRegs per thread;
-  // with fewer, a warpgroup's increase could never be satisfied
-  cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D>);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  // once per device: the register split assumes the kernel launches with
+  // kLaunchRegs per thread (with fewer, a warpgroup's increase could never be
+  // satisfied); the dynamic shared memory; the SM count
+  static OncePerDevice setup;
+  static std::atomic<int> sm_count[64];
+  cudaError_t e = setup.run([](int dev) -> cudaError_t {
+    cudaFuncAttributes fa;
+    cudaError_t r = cudaFuncGetAttributes(&fa, prefill_kernel<D>);
+    if (r != cudaSuccess) return r;
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    r = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (r != cudaSuccess) return r;
+    int n = 0;
+    r = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (r == cudaSuccess && dev < 64) sm_count[dev].store(n);
+    return r;
+  });
   if (e != cudaSuccess) return e;
   // persistent grid: one CTA per SM (the kernel holds an SM's whole TMEM),
   // each walking its share of the item list
   int dev = 0, sms = 0;
   e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
+  if (dev < 64) sms = sm_count[dev].load();
+  if (sms == 0) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
   const int grid = a.n_items < sms ? a.n_items : sms;
   prefill_kernel<D><<<grid, kThreads, smem, s>>>(p, *a.q_map, *a.k_map, *a.v_map);
   return cudaGetLastError();
