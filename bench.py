@@ -121,7 +121,24 @@ def load_peaks():
 
 # --------------------------------------------------------------- algorithmic work
 
-def stage_work(w, fp8=False):
+def prefill_request_mask(w, cfg, opts):
+    """Which requests the plan runs on the prefill kernel (read from the
+    plan's own work list: the planner may also give it short requests)."""
+    from continuous_batching_paged_varlen_gb300 import binding as B
+    hp = B.HostPlan(w.requests, w.block_table, cfg, opts)
+    try:
+        n = hp.info.n_prefill_items
+        off = hp.layout()[2]
+        meta = np.frombuffer(hp.metadata(), dtype=np.uint8)
+        recs = np.frombuffer(meta[off:off + 32 * n].tobytes(), dtype=np.int32).reshape(n, 8)
+    finally:
+        hp.close()
+    mask = np.zeros(len(w.requests), dtype=bool)
+    mask[np.unique(recs[:, 0])] = True  # field 0: the request (block-table row)
+    return mask
+
+
+def stage_work(w, fp8=False, prefill_mask=None):
     """Algorithmic FLOPs and bytes of the two attention kernels' request sets
     (fp8: every request on the split-KV kernel, 1-byte K/V + fp32 row scales)."""
     s = w.spec
@@ -129,12 +146,13 @@ def stage_work(w, fp8=False):
     m = reqs[:, 1] - reqs[:, 0]
     split_min = (1 << 30) if fp8 else PREFILL_MIN_ROWS
     kvb = dict(kv_elem_bytes=1, kv_row_scale_bytes=4) if fp8 else {}
-    pre = reqs[m >= split_min]
-    dec_idx = np.nonzero((m > 0) & (m < split_min))[0]
+    on_pre = (m >= split_min) if prefill_mask is None else (prefill_mask & (m > 0))
+    pre = reqs[on_pre]
+    dec_idx = np.nonzero((m > 0) & ~on_pre)[0]
     dec = reqs[dec_idx]
     out = {}
     out["prefill_flops"] = C.attention_flops(pre, s.n_q_heads, s.head_dim) if len(pre) else 0
-    out["prefill_bytes"] = (C.attention_bytes(pre, w.block_table[m >= split_min],
+    out["prefill_bytes"] = (C.attention_bytes(pre, w.block_table[on_pre],
                                               s.n_q_heads, s.n_kv_heads, s.head_dim,
                                               s.page_size, **kvb) if len(pre) else 0)
     out["decode_flops"] = C.attention_flops(dec, s.n_q_heads, s.head_dim) if len(dec) else 0
@@ -538,7 +556,7 @@ def run_gpu(args):
 
     # ---- roofline of the dominant kernel
     peaks = load_peaks()
-    work = stage_work(w, fp8=args.fp8)
+    work = stage_work(w, fp8=args.fp8, prefill_mask=prefill_request_mask(w, cfg, opts))
     if args.rope:
         work["append_bytes"] = C.rope_append_bytes(w.total_q, s.n_q_heads, s.n_kv_heads,
                                                    s.head_dim)
