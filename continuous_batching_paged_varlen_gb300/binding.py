@@ -138,6 +138,8 @@ def lib():
     L.mb_plan_layout.argtypes = [_vp, ctypes.POINTER(ctypes.c_size_t)]
     L.mb_attn_destroy.restype = ctypes.c_int
     L.mb_attn_destroy.argtypes = [_vp]
+    L.mb_selftest_wait_timeout.restype = ctypes.c_int
+    L.mb_selftest_wait_timeout.argtypes = [_vp, _vp]
     L.mb_attn_forward_noalloc.restype = ctypes.c_int
     L.mb_attn_forward_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
     L.mb_sched_create.restype = ctypes.c_int
@@ -197,6 +199,14 @@ def slot_mapping(requests, block_table, cfg: Config, total_q: int) -> np.ndarray
                                 ctypes.byref(cfg), out.ctypes.data, total_q),
           "mb_slot_mapping")
     return out[:total_q]
+
+
+def selftest_wait_timeout(status, stream=None):
+    """``mb_selftest_wait_timeout``: one CTA's bounded wait on an mbarrier
+    nothing completes runs out; it sets bit ``1 << MB_ERR_TIMEOUT`` in
+    ``status`` (device int32) and returns. Read the status after a sync."""
+    check(lib().mb_selftest_wait_timeout(_ptr(status), _stream_ptr(stream)),
+          "mb_selftest_wait_timeout")
 
 
 def kv_append(k_cache, v_cache, k_new, v_new, slots, cfg: Config, status=None, stream=None):

@@ -10,6 +10,7 @@
 
 #include "../../include/mb.h"
 #include "kernels.h"
+#include "mb_device.cuh"
 #include "mb_internal.h"
 #include "plan_impl.h"
 
@@ -50,9 +51,30 @@ bool make_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* di
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// One CTA waits, with the kernels' bounded wait, on an mbarrier that nothing
+// completes: the wait gives up after its time limit, flags MB_ERR_TIMEOUT and
+// the kernel returns.
+__global__ void wait_timeout_kernel(int32_t* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    dev::mbar_init(&bar, 1);
+    abort_flag = 0;
+    dev::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) dev::mbar_wait(&bar, 0u, &abort_flag, status);
+}
+
 }  // namespace
 
 extern "C" {
+
+mb_status_t mb_selftest_wait_timeout(int32_t* status_dev, cudaStream_t stream) {
+  if (!status_dev || (reinterpret_cast<uintptr_t>(status_dev) & 3)) return MB_ERR_INVALID_ARG;
+  wait_timeout_kernel<<<1, 32, 0, stream>>>(status_dev);
+  return cudaGetLastError() == cudaSuccess ? MB_OK : MB_ERR_CUDA;
+}
 
 mb_status_t mb_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                          const int32_t* slot_mapping, int32_t T, const mb_config_t* cfg,

@@ -133,6 +133,15 @@ typedef struct mb_plan mb_plan_t;
 int32_t mb_abi_version(void);
 const char* mb_status_string(mb_status_t s);
 
+/* Self-test of the failure path every kernel's waits share (no counterpart
+ * on the pages). Launches one CTA on stream whose bounded wait, on an
+ * mbarrier that nothing completes, runs out after the kernels' 2 s limit; the
+ * CTA then sets bit (1 << MB_ERR_TIMEOUT) in *status_dev (device int32,
+ * 4-byte aligned) and returns, as a timed-out attention kernel does: no
+ * fault, and the context stays usable. Returns MB_ERR_INVALID_ARG for a null status_dev,
+ * MB_ERR_CUDA if the launch fails; the caller reads the status after a sync. */
+mb_status_t mb_selftest_wait_timeout(int32_t* status_dev, cudaStream_t stream);
+
 /* Host helper: the slot ("out_cache_loc") of every new row, i.e. where
  * mb_kv_append writes it ("GLM-5.3 e2e token ledger", stage 4).
  * New row t of request r sits at logical position p = kv_length - q_rows +

@@ -250,3 +250,25 @@ def test_split_rows_merged_on_every_forward(name, opts):
     for r in range(w.n_requests):
         if w.requests[r, 1] > w.requests[r, 0]:
             assert_request_close(w, out, lse, r, heads=range(0, s.n_q_heads, 7))
+
+
+def test_bounded_wait_runs_out_and_the_context_stays_usable():
+    """Failure path shared by every kernel's waits: a wait on an mbarrier that
+    nothing completes gives up after its limit (2 s), flags MB_ERR_TIMEOUT in
+    the status word and the kernel returns; the next forward runs normally."""
+    import time
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    B.selftest_wait_timeout(status)
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert int(status.item()) == 1 << B.MB_ERR_TIMEOUT
+    assert 1.5 < waited < 30.0
+    w = W.make_workload("tiny_mixed")
+    kc, vc, cfg = fill_cache(w)
+    out, lse, st, _ = run_forward(w, kc, vc, cfg)
+    assert st == 0
+    for r in range(w.n_requests):
+        if w.requests[r, 1] > w.requests[r, 0]:
+            assert_request_close(w, out, lse, r)
