@@ -20,10 +20,11 @@ LIB_PATH = os.path.join(_PKG, "libmb.so")
 MB_OK = 0
 STATUS_NAMES = {0: "MB_OK", 1: "MB_ERR_INVALID_ARG", 2: "MB_ERR_SHAPE",
                 3: "MB_ERR_UNSUPPORTED", 4: "MB_ERR_WORKSPACE", 5: "MB_ERR_CUDA",
-                6: "MB_ERR_TIMEOUT", 7: "MB_ERR_DEVICE_INDEX"}
+                6: "MB_ERR_TIMEOUT", 7: "MB_ERR_DEVICE_INDEX", 8: "MB_ERR_SHARED_PAGE"}
 MB_ERR_WORKSPACE = 4
 MB_ERR_TIMEOUT = 6
 MB_ERR_DEVICE_INDEX = 7
+MB_ERR_SHARED_PAGE = 8
 STAGE_DECODE, STAGE_COMBINE, STAGE_PREFILL, NUM_STAGES = 0, 1, 2, 3
 
 
@@ -138,6 +139,9 @@ def lib():
     L.mb_plan_layout.argtypes = [_vp, ctypes.POINTER(ctypes.c_size_t)]
     L.mb_attn_destroy.restype = ctypes.c_int
     L.mb_attn_destroy.argtypes = [_vp]
+    L.mb_check_append_targets.restype = ctypes.c_int
+    L.mb_check_append_targets.argtypes = [_vp, _i32, _vp, ctypes.POINTER(Config),
+                                          ctypes.POINTER(_i32)]
     L.mb_selftest_wait_timeout.restype = ctypes.c_int
     L.mb_selftest_wait_timeout.argtypes = [_vp, _vp]
     L.mb_attn_forward_noalloc.restype = ctypes.c_int
@@ -199,6 +203,18 @@ def slot_mapping(requests, block_table, cfg: Config, total_q: int) -> np.ndarray
                                 ctypes.byref(cfg), out.ctypes.data, total_q),
           "mb_slot_mapping")
     return out[:total_q]
+
+
+def check_append_targets(requests, block_table, cfg: Config):
+    """``mb_check_append_targets``: (status, first offending request or -1);
+    MB_ERR_SHARED_PAGE when a new row would land in a page another request
+    also maps."""
+    reqs = _host_i32(requests).reshape(-1, 3)
+    bt = _host_i32(block_table)
+    bad = _i32(-1)
+    st = lib().mb_check_append_targets(reqs.ctypes.data, reqs.shape[0], bt.ctypes.data,
+                                       ctypes.byref(cfg), ctypes.byref(bad))
+    return int(st), int(bad.value)
 
 
 def selftest_wait_timeout(status, stream=None):

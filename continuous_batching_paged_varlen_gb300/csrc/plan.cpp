@@ -580,6 +580,7 @@ const char* mb_status_string(mb_status_t s) {
     case MB_ERR_CUDA: return "CUDA runtime error";
     case MB_ERR_TIMEOUT: return "a bounded device wait ran out";
     case MB_ERR_DEVICE_INDEX: return "device-side index out of range";
+    case MB_ERR_SHARED_PAGE: return "a new row would be written into a shared page";
   }
   return "unknown status";
 }
@@ -604,6 +605,41 @@ mb_status_t mb_slot_mapping(const mb_request_t* reqs, int32_t n_reqs,
       const int32_t p = s0 + (t - q.q_start);
       const int32_t page = block_table_host[(size_t)r * mb + p / ps];
       slots_out[t] = page * ps + p % ps;
+    }
+  }
+  return MB_OK;
+}
+
+mb_status_t mb_check_append_targets(const mb_request_t* reqs, int32_t n_reqs,
+                                    const int32_t* block_table_host, const mb_config_t* cfg,
+                                    int32_t* bad_request_out) {
+  if (bad_request_out) *bad_request_out = -1;
+  mb_status_t st = validate_config(cfg);
+  if (st != MB_OK) return st;
+  int32_t tq = 0;
+  st = validate_requests(reqs, n_reqs, block_table_host, cfg, &tq);
+  if (st != MB_OK) return st;
+  const int ps = cfg->page_size, mb = cfg->max_blocks_per_req;
+  // how many requests map each page (a request mapping a page twice counts once)
+  std::vector<int32_t> maps((size_t)cfg->num_pages, 0), last((size_t)cfg->num_pages, -1);
+  for (int32_t r = 0; r < n_reqs; ++r) {
+    const int32_t nb = (reqs[r].kv_length + ps - 1) / ps;
+    for (int32_t b = 0; b < nb; ++b) {
+      const int32_t page = block_table_host[(size_t)r * mb + b];
+      if (last[(size_t)page] != r) {
+        last[(size_t)page] = r;
+        ++maps[(size_t)page];
+      }
+    }
+  }
+  for (int32_t r = 0; r < n_reqs; ++r) {
+    const int32_t s0 = reqs[r].kv_length - (reqs[r].q_end - reqs[r].q_start);
+    if (reqs[r].q_end == reqs[r].q_start) continue;
+    for (int32_t b = s0 / ps; b <= (reqs[r].kv_length - 1) / ps; ++b) {
+      if (maps[(size_t)block_table_host[(size_t)r * mb + b]] > 1) {
+        if (bad_request_out) *bad_request_out = r;
+        return MB_ERR_SHARED_PAGE;
+      }
     }
   }
   return MB_OK;

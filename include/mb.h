@@ -68,7 +68,9 @@ typedef enum {
   MB_ERR_WORKSPACE = 4,    /* workspace missing, too small or misaligned     */
   MB_ERR_CUDA = 5,         /* a CUDA runtime call failed                     */
   MB_ERR_TIMEOUT = 6,      /* device flag: a bounded wait in a kernel ran out */
-  MB_ERR_DEVICE_INDEX = 7  /* device flag: slot / page index out of range    */
+  MB_ERR_DEVICE_INDEX = 7, /* device flag: slot / page index out of range    */
+  MB_ERR_SHARED_PAGE = 8   /* mb_check_append_targets: a new row would land in
+                              a page another request also maps              */
 } mb_status_t;
 
 /* One request of the iteration ("ORCA and chunked prefill", section 2).
@@ -164,6 +166,18 @@ mb_status_t mb_slot_mapping(const mb_request_t* reqs, int32_t n_reqs,
 mb_status_t mb_positions(const mb_request_t* reqs, int32_t n_reqs, int32_t* positions_out,
                          int32_t total_q);
 
+/* Host debug check of the append contract below: no new row of this
+ * iteration may land in a page that another request's block table also maps
+ * (a shared prefix page is read by every sharer; writing it would change
+ * their history). Request r maps pages block_table_host[r][0 ..
+ * ceil(kv_length / page_size)); its new rows are its positions [kv_length -
+ * q_rows, kv_length). Returns MB_OK, or MB_ERR_SHARED_PAGE with
+ * *bad_request_out = the first offending request (else -1); the errors of
+ * mb_attn_plan for inconsistent inputs. Host only, no CUDA call. */
+mb_status_t mb_check_append_targets(const mb_request_t* reqs, int32_t n_reqs,
+                                    const int32_t* block_table_host,
+                                    const mb_config_t* cfg, int32_t* bad_request_out);
+
 /* KV append: scatter this iteration's K/V rows into their pages
  * ("ORCA and chunked prefill", section 4: append K, V to the cache before
  * the attention reads it). For t in [0, T): slot = slot_mapping[t];
@@ -171,7 +185,8 @@ mb_status_t mb_positions(const mb_request_t* reqs, int32_t n_reqs, int32_t* posi
  *   k_cache[slot / ps][h][slot % ps][:] = k_new[t][h][:]  (same for V),
  * a bit-exact copy. k_new/v_new [T, Hkv, D] contiguous bf16 (device);
  * slot_mapping int32 [T] (device). Pages written here must not be shared
- * with another request (the caller's contract). A slot >= num_pages*ps is
+ * with another request (the caller's contract; mb_check_append_targets
+ * checks it on the host). A slot >= num_pages*ps is
  * skipped and sets bit (1 << MB_ERR_DEVICE_INDEX) in *status_dev
  * (nullable device int32). T = 0 enqueues nothing. Asynchronous on stream. */
 mb_status_t mb_kv_append(void* k_cache, void* v_cache, const void* k_new,

@@ -239,6 +239,35 @@ def test_prefill_tiles_skip_masked_tiles(L):
     assert np.all(np.diff(pitems["n_kv_tiles"]) <= 0)
 
 
+@pytest.mark.parametrize("name", W.ORDER)
+def test_append_targets_are_private_pages_in_every_workload(L, name):
+    w = W.make_workload(name, with_values=False)
+    assert B.check_append_targets(w.requests, w.block_table, cfg_for(w)) == (B.MB_OK, -1)
+
+
+def test_append_into_a_shared_page_is_flagged(L):
+    # requests 0 and 1 share page 5 as their first block; request 1's new row
+    # (position 10 of page 5, page size 16) would be written into it
+    reqs = np.array([[0, 1, 20], [1, 2, 11], [2, 3, 40]], np.int32)
+    bt = np.array([[5, 6, 0], [5, 9, 0], [1, 2, 3]], np.int32)
+    cfg = B.config(4, 2, 64, 16, 10, 3, 0.0)
+    assert B.check_append_targets(reqs, bt, cfg) == (B.MB_ERR_SHARED_PAGE, 1)
+    # request 1 now appends at position 16 (page 9, its own): fine; request 0's
+    # new row at 19 is in page 6, also its own
+    reqs[1] = [1, 2, 17]
+    assert B.check_append_targets(reqs, bt, cfg) == (B.MB_OK, -1)
+    # a page mapped twice by the same request counts as one mapping
+    bt2 = bt.copy()
+    bt2[2] = [1, 1, 3]
+    reqs2 = np.array([[0, 1, 20], [1, 2, 17], [2, 3, 20]], np.int32)
+    assert B.check_append_targets(reqs2, bt2, cfg) == (B.MB_OK, -1)
+    # only a shared page that receives a row counts: request 0 maps page 5 but
+    # appends nothing; request 2 maps it too and appends into page 3
+    reqs4 = np.array([[0, 0, 16], [0, 1, 11], [1, 2, 40]], np.int32)
+    bt4 = np.array([[5, 0, 0], [6, 0, 0], [5, 7, 3]], np.int32)
+    assert B.check_append_targets(reqs4, bt4, cfg) == (B.MB_OK, -1)
+
+
 # ---------------------------------------------------------------- rotary helpers
 
 def test_rope_table_matches_oracle(L):

@@ -89,6 +89,8 @@ def check_iteration(sched, it, before, ps):
     np.testing.assert_array_equal(it.slots, B.slot_mapping(it.requests, it.block_table, ccfg,
                                                            it.total_q))
     np.testing.assert_array_equal(it.positions, B.positions(it.requests, it.total_q))
+    # the append contract: no new row lands in a page another request maps
+    assert B.check_append_targets(it.requests, it.block_table, ccfg) == (B.MB_OK, -1)
     # pages: shared between requests only with a reference count to match
     refs = sched.page_refs()
     owners = {}
