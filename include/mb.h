@@ -126,7 +126,9 @@ typedef struct {
 
 typedef struct mb_plan mb_plan_t;
 
-/* Stages timed by mb_attn_forward_timed, in launch order. */
+/* Stages timed by mb_attn_forward_timed. MB_STAGE_COMBINE is kept for the
+ * event layout: the log-sum-exp merge of split rows runs inside the split-KV
+ * kernel, so its two events are recorded back to back (an empty interval). */
 #define MB_STAGE_DECODE 0
 #define MB_STAGE_COMBINE 1
 #define MB_STAGE_PREFILL 2
@@ -233,8 +235,8 @@ mb_status_t mb_attn_forward_fp8(const mb_plan_t* plan, const void* q,
                                 const int32_t* block_table_dev, void* out,
                                 float* lse, cudaStream_t stream);
 
-/* mb_attn_forward_fp8 with per-stage events (MB_STAGE_DECODE, MB_STAGE_COMBINE),
- * as mb_attn_forward_timed. */
+/* mb_attn_forward_fp8 with per-stage events (MB_STAGE_DECODE; MB_STAGE_COMBINE
+ * empty, as in mb_attn_forward_timed). */
 mb_status_t mb_attn_forward_fp8_timed(const mb_plan_t* plan, const void* q,
                                       const void* k_codes, const void* v_codes,
                                       const float* k_scale, const float* v_scale,
