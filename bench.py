@@ -48,6 +48,7 @@ UNIT = "Q rows/s"
 DEFAULT_WORKLOAD = "llama2_7b_orca_iteration"
 PREFILL_MIN_ROWS = 16  # the planner's default split between the two kernels
 FLUSH_BYTES = 256 << 20
+SPIN_CYCLES = 1_000_000  # ~0.5 ms of device spin before each per-stage pass
 STAGES = ["decode", "prefill"]  # the LSE merge runs inside the split-KV kernels
 STAGE_INDEX = {"decode": 0, "prefill": 2}  # MB_STAGE_DECODE, MB_STAGE_PREFILL
 KERNEL_SOURCES = {"prefill": "prefill.cu", "decode": "decode.cu", "decode_fp8": "decode_fp8.cu"}
@@ -360,7 +361,11 @@ def workload_config(w):
             "head_dim": s.head_dim, "page_size": s.page_size,
             "l2": "flushed between timed steps (256 MiB written, then another 256 MiB read so "
                   "that no dirty line is left to write back; outside the events)",
-            "step": "mb_kv_append + mb_attn_plan (host + 1 H2D) + mb_attn_forward"}
+            "step": "mb_kv_append + mb_attn_plan (host + 1 H2D) + mb_attn_forward",
+            "stage_timing": "per-kernel times from a second pass with CUDA events around each "
+                            "stage, stages back to back, L2 flushed, a 0.5 ms device spin "
+                            "before each pass so the events bracket execution, not host launch "
+                            "gaps"}
 
 
 def workload_config_args(w, args):
@@ -480,7 +485,11 @@ def run_gpu(args):
         plan.close()
 
     def kernel_pass(stage_events, append_events):
-        # the same launches with per-stage events (stages back to back)
+        # the same launches with per-stage events (stages back to back). A
+        # device spin first (torch's, about half a millisecond) lets the host
+        # enqueue the whole pass before the GPU reaches it, so each event pair
+        # brackets its kernel's execution, not the host's launch work.
+        torch.cuda._sleep(SPIN_CYCLES)
         append_events[0].record(stream)
         append()
         append_events[1].record(stream)
