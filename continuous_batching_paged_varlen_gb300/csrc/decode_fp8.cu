@@ -37,7 +37,12 @@
 //               words per task, times the key's vs / rho, into the operand
 //               tiles of a 2-slot ring (rows past k_end zeroed).
 //   warp 9      TMEM allocation; one lane issues S = Q K^T (the hi and lo
-//               rows of Q from TMEM) and O += P' V (P' from TMEM).
+//               rows of Q from TMEM) and O += P' V (P' from TMEM). S has one
+//               buffer: S(j+1) is issued, ahead of PV(j), as soon as the
+//               softmax warps have read S(j) into registers. P has two (by
+//               tile parity), so the softmax of tile j waits only for
+//               PV(j-2) before writing its P (and for PV(j-1) when it must
+//               rescale O).
 //   warps 0-3   softmax; each thread first writes its query row's hi / lo
 //               codes to TMEM. With few rows (a decode step's g query heads),
 //               each row is copied into 4 (or 2) TMEM lanes of different
@@ -65,26 +70,27 @@ constexpr int BM = 128;  // TMEM lanes (query rows, possibly copied)
 constexpr int BN = 128;  // keys per tile
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;    // + 128 * buffer
+constexpr uint32_t kColS = 0;    // S: one 128-key tile, read out by the softmax before S(j+1)
 constexpr uint32_t kColO = 256;  // D columns
 constexpr uint32_t kColQ = 384;  // hi codes (D / 4 columns), then lo codes
-constexpr uint32_t kColP = 448;  // P: 64 columns of f16x2 (128 keys), kept between tiles
+constexpr uint32_t kColP = 128;  // P: two buffers of 64 f16x2 columns (128 keys), by tile parity
 constexpr float kRescaleThreshold = 8.0f;
 constexpr uint64_t kDrainNs = 200000000ull;
-constexpr int kVOpSlots = 2;          // f16 V operand tiles
+constexpr int kVOpSlots = 2;          // f16 V operand tiles: V_j in slot j % 2, freed by PV(j)'s
+                                      // barrier of the same parity (B_O_DONE + j % 2)
 constexpr int kMaxSlots = 8;
 
 enum {
   B_K_FULL = 0,                          // + K slot
-  B_K_EMPTY = B_K_FULL + kMaxSlots,      // + K slot (MMA commit + 4 softmax warps)
+  B_K_EMPTY = B_K_FULL + kMaxSlots,      // + K slot (the 4 softmax warps, after S(j))
   B_VS_FULL = B_K_EMPTY + kMaxSlots,     // + V staging slot
   B_VS_EMPTY = B_VS_FULL + kMaxSlots,    // + V staging slot
-  B_VO_FULL = B_VS_EMPTY + kMaxSlots,    // + V operand slot
-  B_VO_EMPTY = B_VO_FULL + kVOpSlots,    // + V operand slot
-  B_S_FULL = B_VO_EMPTY + kVOpSlots,     // + S buffer
-  B_P_FULL = B_S_FULL + 2,
-  B_O_DONE = B_P_FULL + 1,
-  B_RHO_READY = B_O_DONE + 1,            // converters' partial maxima of the V scales
+  B_S_FULL = B_VS_EMPTY + kMaxSlots,     // S(j) computed
+  B_S_FREE = B_S_FULL + 1,               // the 4 softmax warps have read S(j) out
+  B_PV_READY = B_S_FREE + 1,             // + P buffer: P(j) written (4 softmax warps) and
+                                         // V_j converted (4 converter warps), j of that parity
+  B_O_DONE = B_PV_READY + 2,             // + P buffer: P(j) V(j) done, j of that parity
+  B_RHO_READY = B_O_DONE + 2,            // converters' partial maxima of the V scales
   B_EPI_FULL = B_RHO_READY + 1,
   B_Q_READY = B_EPI_FULL + 1,
   B_MMA_DONE = B_Q_READY + 1,
@@ -109,7 +115,7 @@ struct Layout {
   static constexpr uint32_t redl_off = redm_off + 4 * 32 * 4;             // float [4][32]
   static constexpr uint32_t bar_off = redl_off + 4 * 32 * 4;
   // TMEM address, abort flag, the converters' 4 partial maxima of the V scales
-  static constexpr uint32_t misc_off = bar_off + B_COUNT * 8;
+  static constexpr uint32_t misc_off = (bar_off + B_COUNT * 8 + 15) & ~15u;
   static constexpr uint32_t kBytes = misc_off + 32;
   // more than half the SM so that one CTA holds the SM's 512 TMEM columns
   static constexpr uint32_t kAlloc =
@@ -117,6 +123,7 @@ struct Layout {
   // the epilogue adds the row copies' outputs in the (then idle) K ring
   static constexpr int kRedRow = D + 4;  // floats per row, padded against bank conflicts
   static_assert(kKSlots <= kMaxSlots && kVStSlots <= kMaxSlots, "rings");
+  static_assert(kVOpSlots == 2, "V operand slots are freed by the P-buffer barriers");
   static_assert(4 * 32 * kRedRow * 4 <= kKSlots * kKSlot, "reduction buffer");
   static_assert(kAlloc <= 232448, "shared memory");
   static_assert(misc_off % 16 == 0, "misc alignment");
@@ -303,8 +310,8 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
       uint32_t zero[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) zero[e] = 0u;
-      tmem_st32(sh.tmem + lane_addr + kColP, zero);
-      tmem_st32(sh.tmem + lane_addr + kColP + 32, zero);
+#pragma unroll
+      for (int z = 0; z < 4; ++z) tmem_st32(sh.tmem + lane_addr + kColP + 32 * z, zero);
     }
     tmem_st_wait();
     tc_fence_before();
@@ -321,15 +328,21 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
   bool ok = true;
   for (int j = 0; j < n; ++j) {
     const int ks_slot = j % L::kKSlots;
-    const uint32_t p_col = sh.tmem + lane_addr + kColS + 128 * (j & 1);
-    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_S_FULL + (j & 1)], (uint32_t)(j >> 1) & 1u,
-                                           sh.abort_flag, a.status));
+    const uint32_t p_col = sh.tmem + lane_addr + kColS;
+    const uint32_t p_buf = p_base + 64 * (j & 1);  // this tile's P buffer
+    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_S_FULL], (uint32_t)j & 1u, sh.abort_flag,
+                                           a.status));
     if (!ok) break;
     tc_fence_after();
-    // the K tile's scales arrived with its codes
-    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_K_FULL + ks_slot],
-                                           (uint32_t)(j / L::kKSlots) & 1u, sh.abort_flag,
-                                           a.status));
+    // K_j (its scales arrive with its codes) and K_(j+1): the MMA thread
+    // issues S(j+1) on this warp's release of S(j) alone. K_j was waited
+    // for one tile earlier, except the first.
+    for (int jj = j == 0 ? 0 : j + 1; jj <= j + 1 && jj < n; ++jj) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_K_FULL + jj % L::kKSlots],
+                                             (uint32_t)(jj / L::kKSlots) & 1u, sh.abort_flag,
+                                             a.status));
+      if (!ok) break;
+    }
     if (!ok) break;
     // scores in the log2 domain: ks_j sq log2(e) scale (qc . kcode_j), keys
     // past the row's visibility bound at -inf
@@ -363,6 +376,14 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
 #pragma unroll
       for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(x[e]));
     }
+    // S is in registers: S(j+1) may overwrite it (W = 128 reads it again
+    // below); K_(j+1) has landed (waited for above)
+    auto s_free = [&]() {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_S_FREE]);
+    };
+    if constexpr (W <= 64) s_free();
     const float m_new = fmaxf(m, mx);
     float alpha = 1.f;
     bool need = false;
@@ -393,11 +414,17 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
         pk[2 * e4 + 1] = pack_f16x2(p2, p3);
       }
     };
-    // P(j-1) V(j-1) done: P may be rewritten and O rescaled; waiting every
-    // tile also keeps this barrier's phases in step
+    // P(j-2) V(j-2) done: this tile's P buffer may be rewritten; when the
+    // warp rescales O, P(j-1) V(j-1) too (O is stable; P has two buffers, so
+    // it may still run otherwise). Each P buffer's barrier completes every
+    // other tile and is waited for at every completion, so no wait is two
+    // phases ahead.
+    const bool rescale = j > 0 && __any_sync(0xffffffffu, need);
     auto wait_pv = [&]() -> bool {
-      if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE], (uint32_t)(j - 1) & 1u,
-                                                       sh.abort_flag, a.status)))
+      const int jj = rescale ? j - 1 : j - 2;  // the PV that must be done
+      if (jj >= 0 && !__all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + (jj & 1)],
+                                                        (uint32_t)(jj >> 1) & 1u, sh.abort_flag,
+                                                        a.status)))
         return false;
       tc_fence_after();
       return true;
@@ -409,7 +436,7 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
       for (int h = 0; h < kChunks; ++h) exps(&s[32 * h], &pk[16 * h]);
       if (!(ok = wait_pv())) break;
 #pragma unroll
-      for (int h = 0; h < kChunks; ++h) tmem_st16(p_base + (col0 >> 1) + 16 * h, &pk[16 * h]);
+      for (int h = 0; h < kChunks; ++h) tmem_st16(p_buf + (col0 >> 1) + 16 * h, &pk[16 * h]);
     } else {
       // second pass over S, 32 keys at a time, straight into P
       if (!(ok = wait_pv())) break;
@@ -418,13 +445,15 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
         uint32_t pk[16];
         scaled_chunk(h, s);
         exps(s, pk);
-        tmem_st16(p_base + 16 * h, pk);
+        tmem_st16(p_buf + 16 * h, pk);
       }
+      tmem_st_wait();
+      s_free();
     }
     l += sum[0] + sum[1];
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars[B_K_EMPTY + ks_slot]);  // done with the K tile's scales
-    if (j > 0 && __any_sync(0xffffffffu, need)) {
+    if (rescale) {
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -438,11 +467,12 @@ __device__ __forceinline__ void softmax_role(const DecodeFp8Args& a, const Decod
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&bars[B_P_FULL]);
+    if (lane == 0) mbar_arrive(&bars[B_PV_READY + (j & 1)]);
   }
-  if (ok && n > 0)
-    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE], (uint32_t)(n - 1) & 1u,
-                                           sh.abort_flag, a.status));
+  if (ok && n > 0)  // P(n-1) V(n-1) done, and with it every PV before it
+    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + ((n - 1) & 1)],
+                                           (uint32_t)((n - 1) >> 1) & 1u, sh.abort_flag,
+                                           a.status));
   // the V operand carries vs / rho: O = rho * (P V') / l
   if (ok && n > 0)
     ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_RHO_READY], 0u, sh.abort_flag, a.status));
@@ -590,20 +620,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < L::kKSlots; ++s) {
       mbar_init(&bars[B_K_FULL + s], 1);
-      mbar_init(&bars[B_K_EMPTY + s], 5);
+      mbar_init(&bars[B_K_EMPTY + s], 4);
     }
     for (int s = 0; s < L::kVStSlots; ++s) {
       mbar_init(&bars[B_VS_FULL + s], 1);
       mbar_init(&bars[B_VS_EMPTY + s], 4);
     }
-    for (int o = 0; o < kVOpSlots; ++o) {
-      mbar_init(&bars[B_VO_FULL + o], 4);
-      mbar_init(&bars[B_VO_EMPTY + o], 1);
-    }
-    mbar_init(&bars[B_S_FULL + 0], 1);
-    mbar_init(&bars[B_S_FULL + 1], 1);
-    mbar_init(&bars[B_P_FULL], 4);
-    mbar_init(&bars[B_O_DONE], 1);
+    mbar_init(&bars[B_S_FULL], 1);
+    mbar_init(&bars[B_S_FREE], 4);
+    mbar_init(&bars[B_PV_READY + 0], 8);
+    mbar_init(&bars[B_PV_READY + 1], 8);
+    mbar_init(&bars[B_O_DONE + 0], 1);
+    mbar_init(&bars[B_O_DONE + 1], 1);
     mbar_init(&bars[B_RHO_READY], 4);
     mbar_init(&bars[B_EPI_FULL], 4);
     mbar_init(&bars[B_Q_READY], 4);
@@ -748,9 +776,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              (uint32_t)(j / L::kVStSlots) & 1u, abort_flag,
                                              a.status)))
         break;
+      // operand slot j % 2 is free once PV(j-2) is done
       if (j >= kVOpSlots &&
-          !__all_sync(0xffffffffu, mbar_wait(&bars[B_VO_EMPTY + vo],
-                                             ((uint32_t)(j / kVOpSlots) & 1u) ^ 1u, abort_flag,
+          !__all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + (j & 1)],
+                                             (uint32_t)((j >> 1) - 1) & 1u, abort_flag,
                                              a.status)))
         break;
       tc_fence_after();
@@ -802,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&bars[B_VS_EMPTY + vs]);
-        mbar_arrive(&bars[B_VO_FULL + vo]);
+        mbar_arrive(&bars[B_PV_READY + (j & 1)]);  // V_j in operand slot j % 2
       }
     }
   } else if (warp == 9) {
@@ -820,7 +849,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_s = [&](int j) -> bool {
         const int slot = j % L::kKSlots;
-        if (!wait(B_K_FULL + slot, (uint32_t)(j / L::kKSlots) & 1u)) return false;
+        // K_j landed: waited for here for the first tile; for the others the
+        // softmax warps waited before releasing S(j - 1)
+        if (j == 0 && !wait(B_K_FULL + slot, 0u)) return false;
         const uint32_t k0 = ka + slot * L::kKSlot;
 #pragma unroll
         for (int part = 0; part < 2; ++part)  // hi codes, then lo codes of Q
@@ -828,31 +859,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < D / 32; ++kk) {  // 32 e4m3 values (32 bytes) per MMA
             const uint64_t bd = D == 128 ? sdesc_sw128(k0 + kk * 32, 16, 1024)
                                          : sdesc_sw64(k0 + kk * 32, 16, 512);
-            umma_f8_ts(tmem + kColS + 128 * (j & 1), tmem + kColQ + part * (D / 4) + kk * 8, bd,
-                       idesc_qk, (part | kk) ? 1u : 0u);
+            umma_f8_ts(tmem + kColS, tmem + kColQ + part * (D / 4) + kk * 8, bd, idesc_qk,
+                       (part | kk) ? 1u : 0u);
           }
-        umma_commit(&bars[B_S_FULL + (j & 1)]);
-        umma_commit(&bars[B_K_EMPTY + slot]);
+        umma_commit(&bars[B_S_FULL]);
         return true;
       };
       bool ok = n > 0 && wait(B_Q_READY, 0u);
       if (ok) ok = issue_s(0);
-      if (ok && n > 1) ok = issue_s(1);
       for (int j = 0; ok && j < n; ++j) {
+        // S(j+1) overwrites S(j) once the softmax warps have read it out,
+        // ahead of PV(j): the next tile's scores overlap this tile's softmax
+        if (j + 1 < n) {
+          if (!(ok = wait(B_S_FREE, (uint32_t)j & 1u))) break;
+          if (!(ok = issue_s(j + 1))) break;
+        }
         const int vo = j % kVOpSlots;
-        if (!(ok = wait(B_VO_FULL + vo, (uint32_t)(j / kVOpSlots) & 1u))) break;
-        if (!(ok = wait(B_P_FULL, (uint32_t)j & 1u))) break;
+        // P(j) written and V_j converted: one barrier per P buffer (the
+        // softmax may already have written P(j+1) -- S(j+1) went ahead of
+        // PV(j) -- never P(j+2); V_(j+2) waits for PV(j))
+        if (!(ok = wait(B_PV_READY + (j & 1), (uint32_t)(j >> 1) & 1u))) break;
         const uint32_t v0 = voa + vo * L::kVOpBytes;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint64_t bd = sdesc_sw128(v0 + kk * 2048, L::kHalfBytes, 1024);
-          umma_bf16_ts(tmem + kColO, tmem + kColP + kk * 8, bd, idesc_pv,
+          umma_bf16_ts(tmem + kColO, tmem + kColP + 64 * (j & 1) + kk * 8, bd, idesc_pv,
                        (j > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&bars[B_O_DONE]);
-        umma_commit(&bars[B_VO_EMPTY + vo]);
-        // S(j+2) reuses this S buffer; it follows PV(j) in issue order
-        if (j + 2 < n && !(ok = issue_s(j + 2))) break;
+        umma_commit(&bars[B_O_DONE + (j & 1)]);  // also frees V operand slot j % 2
       }
       // everything issued has completed before TMEM is freed
       umma_commit(&bars[B_MMA_DONE]);
