@@ -633,13 +633,16 @@ def run_gpu(args):
 
         # A serving loop keeps steps in flight: step i's upload (its own
         # stream) overlaps step i-1's attention, and its download (a third
-        # stream) overlaps step i+1's upload. Inputs and outputs rotate over
-        # NBUF buffer sets; every step still uploads its Q/K/V and downloads
-        # its O/LSE.
+        # stream) overlaps step i+1's upload. Inputs, outputs and plan
+        # workspaces rotate over NBUF buffer sets; every step still plans,
+        # uploads its Q/K/V and downloads its O/LSE. The plan is made on the
+        # upload stream, ahead of the step's inputs: its work-list copy then
+        # shares the copy engine's queue in order, instead of waiting on the
+        # compute stream behind the next step's 100 MB upload.
         NBUF = 3
         s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         bufs = [dict(q=torch.empty_like(q), k=torch.empty_like(k_new), v=torch.empty_like(v_new),
-                     o=torch.empty_like(out), l=torch.empty_like(lse),
+                     o=torch.empty_like(out), l=torch.empty_like(lse), ws=torch.empty_like(ws),
                      ho=torch.empty(out.shape, dtype=out.dtype).pin_memory(),
                      hl=torch.empty(lse.shape, dtype=lse.dtype).pin_memory(),
                      free=torch.cuda.Event(), up=torch.cuda.Event(), done=torch.cuda.Event())
@@ -650,13 +653,14 @@ def run_gpu(args):
             with torch.cuda.stream(s_up):
                 if i >= NBUF:  # step i-NBUF has been computed and downloaded
                     s_up.wait_event(b["free"])
+                plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=b["ws"],
+                              opts=opts, stream=s_up)
                 b["q"].copy_(hq, non_blocking=True)
                 b["k"].copy_(hk, non_blocking=True)
                 b["v"].copy_(hv, non_blocking=True)
                 b["up"].record(s_up)
             stream.wait_event(b["up"])
             append_rows(b["k"], b["v"], slots)
-            plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=ws, opts=opts)
             forward(plan, b["q"], o=b["o"], l=b["l"])
             plan.close()
             b["done"].record(stream)
@@ -680,9 +684,10 @@ def run_gpu(args):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": piped_ms,
                "timing": "K steps through the public calls, pipelined (each step's Q/K/V "
-                         "upload from pinned host memory on an upload stream, append + plan + "
-                         "forward on the compute stream, O/LSE download on a third stream; "
-                         "inputs and outputs rotate over 3 buffer sets); host wall clock over "
+                         "upload from pinned host memory and its plan on an upload stream, "
+                         "append + forward on the compute stream, O/LSE download on a third "
+                         "stream; inputs, outputs and workspaces rotate over 3 buffer sets); "
+                         "host wall clock over "
                          "the K steps, synchronised at both ends",
                "serial": {"value": world * w.total_q / (statistics.mean(e_ms) / 1e3),
                           "ms_per_step": statistics.mean(e_ms),

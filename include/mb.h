@@ -293,7 +293,12 @@ mb_status_t mb_rope_kv_append(void* q, void* k_cache, void* v_cache, const void*
  * plan is used) receives the work lists with one host->device copy on
  * stream, and *out_plan a new plan (free with mb_attn_destroy). The plan
  * may be reused by any number of mb_attn_forward calls (e.g. every layer
- * of the iteration). */
+ * of the iteration). The copy runs on the host->device copy engine, in the
+ * same queue as the caller's input uploads: a loop that uploads the next
+ * step's inputs on another stream while this step computes should plan each
+ * step on that upload stream, ahead of the step's inputs, with one workspace
+ * per step in flight (planned on the compute stream, the small copy waits
+ * behind the next step's bulk upload). */
 mb_status_t mb_attn_plan(const mb_request_t* reqs, int32_t n_reqs,
                          const int32_t* block_table_host, const mb_config_t* cfg,
                          void* workspace, size_t* workspace_bytes,
