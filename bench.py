@@ -376,6 +376,7 @@ def workload_config_args(w, args):
         c["cascade"] = "disabled"
     if args.rope:
         c["append"] = "fused rotary embedding + KV append (mb_rope_kv_append)"
+        c["step"] = "mb_rope_kv_append + mb_attn_plan (host + 1 H2D) + mb_attn_forward"
     if args.fp8:
         c["kv_cache"] = ("fp8 e4m3 codes + one fp32 scale per (token, KV head) row; "
                          "mb_kv_append_fp8 + mb_attn_forward_fp8, every request on the "
