@@ -106,3 +106,62 @@ def test_captured_iteration_replays_match_the_oracle(name, opts):
             assert_request_close(wr, out, lse, r)
     graph.reset()
     plan.close()
+
+
+def test_captured_fp8_iteration_replays_match_the_oracle():
+    """The same on the fp8 cache: the quantizing append of this iteration's
+    rows and the split-KV forward over the codes (shared-prefix cascade, split
+    rows merged in the kernel), captured once and replayed with new values."""
+    from tests.test_gpu_fp8 import check_all, empty_caches, slots_of
+
+    w = W.make_workload("shared_prefix_decode")
+    cfg = cfg_of(w)
+    s = w.spec
+    ps = s.page_size
+    k8, v8, ks, vs = empty_caches(w)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hs = torch.from_numpy(slots_of(w.hist_requests, w.block_table, ps).astype(np.int32)).cuda()
+    B.kv_append_fp8(k8, v8, ks, vs, w.k_hist.cuda(), w.v_hist.cuda(), hs, cfg, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    plan = B.Plan(w.requests, w.block_table, cfg, device="cuda",
+                  opts=B.options(prefill_min_rows=-1))
+    assert plan.info.n_combine > 0 and plan.info.n_cascade_groups == 1
+
+    q = w.q.cuda()
+    k_new, v_new = w.k_new.cuda(), w.v_new.cuda()
+    slots = torch.from_numpy(slots_of(w.requests, w.block_table, ps).astype(np.int32)).cuda()
+    bt = torch.from_numpy(np.ascontiguousarray(w.block_table)).cuda()
+    out = torch.zeros((w.total_q, s.n_q_heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((w.total_q, s.n_q_heads), dtype=torch.float32, device="cuda")
+
+    def iteration():
+        B.kv_append_fp8(k8, v8, ks, vs, k_new, v_new, slots, cfg, st)
+        plan.forward_fp8(q, k8, v8, ks, vs, bt, out, lse)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        iteration()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        iteration()
+    torch.cuda.synchronize()
+
+    for replay, seed in enumerate((404, 505)):
+        wr = _fresh_values(w, seed)
+        q.copy_(wr.q)
+        k_new.copy_(wr.k_new)
+        v_new.copy_(wr.v_new)
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        assert plan.device_status() == 0, f"replay {replay}"
+        check_all(wr, out, lse)
+    graph.reset()
+    plan.close()
