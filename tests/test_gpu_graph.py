@@ -1,8 +1,9 @@
 """An iteration's launches captured once in a CUDA graph and replayed.
 
-A serving loop keeps its buffers static and replays a captured graph instead
-of launching each kernel from the host (the ORCA / SGLang style iteration on
-the "Continuous batching" pages: static buffers, graph capture). This file
+A serving loop builds each iteration's inputs into static buffers so that
+the forward can be replayed as a captured CUDA graph instead of launching
+each kernel from the host ("GLM-5.3 e2e token ledger", stage 4: the input
+batch, its slot mapping and block table, CUDA-graph buffers). This file
 captures ``mb_kv_append`` + ``mb_attn_forward`` (the plan is made and
 uploaded beforehand, outside the capture), then writes new Q / K / V values
 into the static input buffers before each replay and checks every replay
