@@ -5,10 +5,14 @@
 // "GLM-5.3 e2e token ledger", stage 4: the host decides, per new token, the
 // page and slot it goes to (out_cache_loc); this kernel only moves bytes.
 //
-// One block per token: its Hkv rows of K and of V are contiguous in k_new /
-// v_new and land in Hkv page rows of ps * D elements apart, so the block's
-// threads walk the token's 16-byte chunks with 32-bit index math, four chunks
-// of K and four of V in flight per thread. The copy is bit-exact.
+// A block takes a group of consecutive tokens (one token when a token's K
+// row set is at least kThreads * U chunks, several when rows are short, so a
+// block always moves a few KB) and walks the group's 16-byte chunks; K and V
+// rows of a token are contiguous in k_new / v_new and land in Hkv page rows
+// ps * D elements apart. Blocks stride over the groups, so a long append
+// (a whole prompt's history) is not bound by the rate at which blocks can
+// be launched. Four chunks of K and four of V are in flight per thread. The
+// copy is bit-exact.
 #include <cuda_runtime.h>
 
 #include "../../include/mb.h"
@@ -19,46 +23,53 @@ namespace mb {
 namespace {
 
 constexpr int kThreads = 128;
+constexpr int kUnroll = 4;
+constexpr int kMaxBlocks = 8192;
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) kv_append_kernel(
     uint4* __restrict__ kc, uint4* __restrict__ vc, const uint4* __restrict__ kn,
-    const uint4* __restrict__ vn, const int32_t* __restrict__ slots, int32_t Hkv,
-    int32_t ps_shift, int64_t n_slots, int32_t* status) {
+    const uint4* __restrict__ vn, const int32_t* __restrict__ slots, int32_t T, int32_t Hkv,
+    int32_t ps_shift, int64_t n_slots, int32_t group, int32_t* status) {
   constexpr int CH = D / 8;  // 16-byte chunks per row
-  const int t = blockIdx.x;
-  const int32_t slot = __ldg(slots + t);
-  if (slot < 0) return;  // padding row
-  if ((int64_t)slot >= n_slots) {
-    if (threadIdx.x == 0) dev::set_status(status, MB_ERR_DEVICE_INDEX);
-    return;
-  }
-  const int32_t page = slot >> ps_shift;
-  const int32_t off = slot & ((1 << ps_shift) - 1);
-  const int n = Hkv * CH;  // chunks of one token's K (and of its V)
-  const uint4* ksrc = kn + (int64_t)t * n;
-  const uint4* vsrc = vn + (int64_t)t * n;
-  // chunk c of head h goes to page row ((page * Hkv + h) << ps_shift) + off
-  const int64_t base = (((int64_t)page * Hkv) << ps_shift) + off;
-  constexpr int U = 4;
-  for (int c0 = threadIdx.x; c0 < n; c0 += kThreads * U) {
-    uint4 kv[U], vv[U];
+  constexpr int U = kUnroll;
+  const int n = Hkv * CH;    // chunks of one token's K (and of its V)
+  const int32_t off_mask = (1 << ps_shift) - 1;
+  for (int64_t t0 = (int64_t)blockIdx.x * group; t0 < T; t0 += (int64_t)gridDim.x * group) {
+    const int nt = (int)(T - t0 < group ? T - t0 : group);
+    const int m = nt * n;  // chunks of this group
+    const uint4* ksrc = kn + t0 * n;
+    const uint4* vsrc = vn + t0 * n;
+    for (int f0 = threadIdx.x; f0 < m; f0 += kThreads * U) {
+      uint4 kv[U], vv[U];
+      int64_t dst[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int c = c0 + u * kThreads;
-      if (c < n) {
-        kv[u] = __ldg(ksrc + c);
-        vv[u] = __ldg(vsrc + c);
+      for (int u = 0; u < U; ++u) {
+        const int f = f0 + u * kThreads;
+        dst[u] = -1;
+        if (f < m) {
+          const int tl = f / n, c = f - tl * n;
+          const int32_t slot = __ldg(slots + t0 + tl);
+          if (slot < 0) continue;  // padding row
+          if ((int64_t)slot >= n_slots) {
+            if (c == 0) dev::set_status(status, MB_ERR_DEVICE_INDEX);
+            continue;
+          }
+          // chunk c (head h, chunk cc of the row) goes to page row
+          // ((page * Hkv + h) << ps_shift) + off
+          const int h = c / CH, cc = c - h * CH;
+          const int64_t row = (((int64_t)(slot >> ps_shift) * Hkv + h) << ps_shift) + (slot & off_mask);
+          dst[u] = row * CH + cc;
+          kv[u] = __ldg(ksrc + f);
+          vv[u] = __ldg(vsrc + f);
+        }
       }
-    }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int c = c0 + u * kThreads;
-      if (c < n) {
-        const int h = c / CH, cc = c - h * CH;
-        const int64_t dst = (base + ((int64_t)h << ps_shift)) * CH + cc;
-        kc[dst] = kv[u];
-        vc[dst] = vv[u];
+      for (int u = 0; u < U; ++u) {
+        if (dst[u] >= 0) {
+          kc[dst[u]] = kv[u];
+          vc[dst[u]] = vv[u];
+        }
       }
     }
   }
@@ -72,14 +83,18 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new,
                              int32_t num_pages, int32_t* status, cudaStream_t s) {
   const int ps_shift = __builtin_ctz((unsigned)page_size);
   const int64_t n_slots = (int64_t)num_pages * page_size;
+  const int n = n_kv_heads * (head_dim / 8);
+  const int group = n >= kThreads * kUnroll ? 1 : (kThreads * kUnroll) / n;
+  const int64_t groups = ((int64_t)T + group - 1) / group;
+  const unsigned grid = (unsigned)(groups < kMaxBlocks ? groups : kMaxBlocks);
   if (head_dim == 128)
-    kv_append_kernel<128><<<(unsigned)T, kThreads, 0, s>>>(
-        (uint4*)k_cache, (uint4*)v_cache, (const uint4*)k_new, (const uint4*)v_new, slots,
-        n_kv_heads, ps_shift, n_slots, status);
+    kv_append_kernel<128><<<grid, kThreads, 0, s>>>(
+        (uint4*)k_cache, (uint4*)v_cache, (const uint4*)k_new, (const uint4*)v_new, slots, T,
+        n_kv_heads, ps_shift, n_slots, group, status);
   else
-    kv_append_kernel<64><<<(unsigned)T, kThreads, 0, s>>>(
-        (uint4*)k_cache, (uint4*)v_cache, (const uint4*)k_new, (const uint4*)v_new, slots,
-        n_kv_heads, ps_shift, n_slots, status);
+    kv_append_kernel<64><<<grid, kThreads, 0, s>>>(
+        (uint4*)k_cache, (uint4*)v_cache, (const uint4*)k_new, (const uint4*)v_new, slots, T,
+        n_kv_heads, ps_shift, n_slots, group, status);
   return cudaGetLastError();
 }
 
