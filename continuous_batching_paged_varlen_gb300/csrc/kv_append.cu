@@ -25,6 +25,7 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kUnroll = 4;
 constexpr int kMaxBlocks = 8192;
+constexpr int kMinBlocks = 2 * 152;  // two blocks per SM before tokens are grouped
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) kv_append_kernel(
@@ -84,7 +85,12 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new,
   const int ps_shift = __builtin_ctz((unsigned)page_size);
   const int64_t n_slots = (int64_t)num_pages * page_size;
   const int n = n_kv_heads * (head_dim / 8);
-  const int group = n >= kThreads * kUnroll ? 1 : (kThreads * kUnroll) / n;
+  // short appends (a decode step's few hundred rows) keep one token per
+  // block so that they still spread over every SM; long ones group tokens
+  // until a block moves kThreads * kUnroll chunks
+  const int group_max = n >= kThreads * kUnroll ? 1 : (kThreads * kUnroll) / n;
+  const int64_t by_size = (int64_t)T / kMinBlocks;
+  const int group = by_size < 1 ? 1 : (by_size < group_max ? (int)by_size : group_max);
   const int64_t groups = ((int64_t)T + group - 1) / group;
   const unsigned grid = (unsigned)(groups < kMaxBlocks ? groups : kMaxBlocks);
   if (head_dim == 128)
