@@ -6,6 +6,7 @@ world x rows per step x steps / the slowest rank's time. The reference arm
 prints only on rank 0; the other ranks exit 0 without work.
 """
 
+import json
 import os
 import socket
 import subprocess
@@ -69,3 +70,29 @@ def test_reference_arm_prints_on_rank_zero_only():
                        capture_output=True, text=True, timeout=300)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def test_reference_arm_line_keeps_the_contract():
+    # rank 0 of the reference arm (the fp64 oracle on the host cores) prints
+    # one JSON line with the GPU arm's metric, unit and config and its own
+    # cpu_baseline / e2e descriptions
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload",
+                        "tiny_mixed", "--steps", "2", "--warmup", "1"], cwd=ROOT,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = [x for x in r.stdout.splitlines() if x.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 1
+    assert d["config"]["workload"] == "tiny_mixed" and d["config"]["q_rows"] == 129
+    assert d["value"] > 0 and d["higher_is_better"] is True
+    assert d["ms_per_step"] == pytest.approx(129 / d["value"] * 1e3)
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert cb["unit"] == d["unit"] and "oracle work" in cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
