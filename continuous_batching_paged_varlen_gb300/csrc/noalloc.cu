@@ -1,7 +1,8 @@
 // Attention forward for callers that cannot allocate device memory.
 //
-// Same kernels and launch order as mb_attn_forward; the difference is where
-// the scratch lives. mb_attn_forward uses a workspace the caller allocated;
+// Same kernels as mb_attn_forward, launched one after the other (split-KV,
+// then prefill) without the overlap mb_attn_forward arranges between them;
+// the other difference is where the scratch lives. mb_attn_forward uses a workspace the caller allocated;
 // this entry point uses g_scratch below, a static device array of
 // MB_NOALLOC_SCRATCH_BYTES that the library owns. The host plan's work lists
 // are copied into it at every call, then the split-KV partials are written
@@ -28,26 +29,63 @@ constexpr float kLog2e = 1.4426950408889634f;
 // One copy per GPU that loads the library, kept until the process exits.
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
+// The array's device address per device, with the id of the CUDA context it
+// was looked up in: a context created later on the same device (after a
+// cudaDeviceReset, say) loads the library's module again, at another address.
+struct ScratchAddr {
+  unsigned long long ctx_id;
+  void* ptr;
+};
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-// Device address of g_scratch on the current device. Host code cannot use
-// the symbol itself as a device pointer, so it is looked up once per device
-// (with that device current) and cached.
+// Id of the calling thread's current CUDA context (driver entry points
+// cuCtxGetCurrent / cuCtxGetId, reached through the runtime).
+bool current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_scratch in the current device's context. Host code
+// cannot use the symbol itself as a device pointer, so the address is looked
+// up (with that device current) once per device and context, and cached.
 mb_status_t scratch_for_current_device(void** out) {
   int device = -1;
   if (cudaGetDevice(&device) != cudaSuccess) return MB_ERR_CUDA;
   if (device < 0 || device >= kMaxDevices) return MB_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_ptr[device]) {
+  ScratchAddr& a = g_scratch_addr[device];
+  unsigned long long ctx = 0;
+  const bool have_ctx = current_context_id(&ctx);
+  if (!have_ctx || !a.ptr || a.ctx_id != ctx) {
+    // the lookup also makes the device's primary context current when no
+    // context is yet
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
     if (e != cudaSuccess || p == nullptr) return MB_ERR_CUDA;
-    g_scratch_ptr[device] = p;
+    if (!have_ctx && !current_context_id(&ctx)) return MB_ERR_CUDA;
+    a.ptr = p;
+    a.ctx_id = ctx;
   }
-  *out = g_scratch_ptr[device];
+  *out = a.ptr;
   return MB_OK;
 }
 
@@ -86,7 +124,13 @@ extern "C" mb_status_t mb_attn_forward_noalloc(const mb_plan_t* plan, const void
   if (!plan) return MB_ERR_INVALID_ARG;
   const PlanDevice& d = plan->dev;
   if (d.workspace_bytes > kScratchBytes) return MB_ERR_WORKSPACE;
-  if (d.total_q == 0) return MB_OK;
+  if (reinterpret_cast<uintptr_t>(status_dev) & 3) return MB_ERR_INVALID_ARG;
+  if (d.total_q == 0) {
+    // nothing to run: the caller's status word still reports "no flags"
+    if (status_dev && cudaMemsetAsync(status_dev, 0, sizeof(int32_t), stream) != cudaSuccess)
+      return MB_ERR_CUDA;
+    return MB_OK;
+  }
   if (!q || !k_cache || !v_cache || !block_table_dev || !out) return MB_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(lse) & 3) ||

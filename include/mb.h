@@ -376,16 +376,23 @@ mb_status_t mb_plan_info(const mb_plan_t* plan, mb_plan_info_t* info);
  * array until the process exits. A plan whose info.workspace_bytes exceeds
  * the array is rejected with MB_ERR_WORKSPACE before anything is enqueued.
  *
- * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture. Each call
- * copies the plan's work lists (from the plan's pageable host memory) into
- * the array on `stream` -- this also clears the device status word -- then
- * launches the same kernels as mb_attn_forward. Every call shares the one
- * array and it keeps the last call's contents: calls whose work overlaps on
- * the GPU (other streams, other host threads) race on it, so serialise them.
- * status_dev (nullable, device int32) receives a copy of the call's device
- * error flags (bits 1 << MB_ERR_TIMEOUT / MB_ERR_DEVICE_INDEX). Inputs,
- * outputs and errors are otherwise as for mb_attn_forward. */
+ * The first call on a device (and the first after that device's CUDA context
+ * was re-created) looks up the array's device address with that device
+ * current; make that first call outside any stream capture. Each call then
+ * copies the plan's work lists into the array with cudaMemcpyAsync on
+ * `stream` -- this also clears the device status word. The source is the
+ * plan's ordinary (pageable) host memory, so the CUDA runtime may make the
+ * calling thread wait until the stream's earlier work has finished before
+ * the copy. The call then launches the same kernels as mb_attn_forward, one
+ * after the other: unlike mb_attn_forward it does not start the split-KV
+ * kernel under the prefill kernel's tail, so a plan with both kinds of work
+ * takes a little longer. Every call shares the one array and it keeps the
+ * last call's contents: calls whose work overlaps on the GPU (other streams,
+ * other host threads) race on it, so serialise them. status_dev (nullable,
+ * device int32, 4-byte aligned) receives a copy of the call's device error
+ * flags (bits 1 << MB_ERR_TIMEOUT / MB_ERR_DEVICE_INDEX), and zero for a plan
+ * with no rows. Inputs, outputs and errors are otherwise as for
+ * mb_attn_forward. */
 #define MB_NOALLOC_SCRATCH_BYTES (8u << 20)
 mb_status_t mb_attn_forward_noalloc(const mb_plan_t* plan, const void* q,
                                     const void* k_cache, const void* v_cache,
