@@ -90,6 +90,9 @@ def parse_args(argv=None):
     ap.add_argument("--fp8", action="store_true",
                     help="fp8 (e4m3) KV cache with per-row fp32 scales: quantizing append "
                          "(mb_kv_append_fp8) and mb_attn_forward_fp8")
+    ap.add_argument("--prefill-ctas", type=int, default=0,
+                    help="planner option: SMs of the prefill grid beside the split-KV kernel "
+                         "(0: the planner's model, < 0: every SM)")
     ap.add_argument("--layers", type=int, default=1,
                     help="a step runs this many layers, each with its own cache: one plan, "
                          "then append + forward per layer, back to back")
@@ -438,12 +441,15 @@ def workload_config_args(w, args, world=1):
         c["max_requests"] = args.max_requests
     if args.disable_cascade:
         c["cascade"] = "disabled"
+    if args.prefill_ctas:
+        c["prefill_ctas"] = args.prefill_ctas
     if args.rope:
         c["append"] = "fused rotary embedding + KV append (mb_rope_kv_append)"
         c["step"] = "mb_rope_kv_append + mb_attn_plan (host + 1 H2D) + mb_attn_forward"
     if args.fp8:
         c["kv_cache"] = ("fp8 e4m3 codes + one fp32 scale per (token, KV head) row; "
-                         "mb_kv_append_fp8 + mb_attn_forward_fp8")
+                         "mb_kv_append_fp8 + mb_attn_forward_fp8 (prefill requests: their "
+                         "pages dequantized to bf16 staging, then the tensor-core kernel)")
         c["step"] = "mb_kv_append_fp8 + mb_attn_plan (host + 1 H2D) + mb_attn_forward_fp8"
     if args.layers > 1:
         c["layers"] = args.layers
@@ -489,16 +495,23 @@ def run_reference(args):
 
 
 def truncate(w, n):
-    """The first n requests of a workload (same pages, same values)."""
+    """The first n requests of a workload, same values, with the page pool
+    cut down to the pages they use (renumbered in the same relative order),
+    so that a small profiling case holds little device memory."""
     import dataclasses
     n = min(n, w.n_requests)
     tq = int(w.requests[n - 1, 1])
     th = int(w.hist_requests[n - 1, 1])
-    return dataclasses.replace(w, requests=w.requests[:n].copy(),
-                               block_table=w.block_table[:n].copy(), q=w.q[:tq],
-                               k_new=w.k_new[:tq], v_new=w.v_new[:tq],
+    bt = w.block_table[:n]
+    used = np.unique(bt[bt >= 0])
+    remap = np.full(w.num_pages, -1, dtype=np.int32)
+    remap[used] = np.arange(len(used), dtype=np.int32)
+    bt = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1).astype(np.int32)
+    return dataclasses.replace(w, requests=w.requests[:n].copy(), block_table=bt,
+                               num_pages=int(len(used)), q=w.q[:tq].clone(),
+                               k_new=w.k_new[:tq].clone(), v_new=w.v_new[:tq].clone(),
                                hist_requests=w.hist_requests[:n].copy(),
-                               k_hist=w.k_hist[:th], v_hist=w.v_hist[:th])
+                               k_hist=w.k_hist[:th].clone(), v_hist=w.v_hist[:th].clone())
 
 
 # --------------------------------------------------------------- GPU arm
@@ -558,11 +571,12 @@ def measure(args, name, dev, local, world, *, main):
     w = W.make_workload(name, device=dev)
     if main and args.max_requests:
         w = truncate(w, args.max_requests)
+        torch.cuda.empty_cache()
     s = w.spec
     opts = None
-    disable_cascade = main and args.disable_cascade
-    if disable_cascade:
-        opts = B.options(disable_cascade=1)
+    if main and (args.disable_cascade or args.prefill_ctas or fp8):
+        opts = B.options(disable_cascade=1 if args.disable_cascade else 0,
+                         prefill_ctas=args.prefill_ctas, fp8_cache=1 if fp8 else 0)
     cfg = B.config(s.n_q_heads, s.n_kv_heads, s.head_dim, s.page_size, w.num_pages,
                    w.block_table.shape[1], s.scale or 0.0)
     shape = (w.num_pages, s.n_kv_heads, s.page_size, s.head_dim)
@@ -730,7 +744,8 @@ def measure(args, name, dev, local, world, *, main):
     if rope:
         work["append_bytes"] = C.rope_append_bytes(w.total_q, s.n_q_heads, s.n_kv_heads,
                                                    s.head_dim)
-    names = {"prefill": "prefill_kernel (tcgen05)",
+    names = {"prefill": ("dequant_pages_kernel + prefill_kernel (tcgen05)" if fp8 else
+                         "prefill_kernel (tcgen05)"),
              "decode": "splitkv_fp8_kernel" if fp8 else "splitkv_kernel",
              "append": ("rope_append_kernel" if rope else
                         "kv_append_fp8_kernel" if fp8 else "kv_append_kernel")}
@@ -927,7 +942,7 @@ def run_gpu(args):
     torch.cuda.empty_cache()
 
     plain = not (args.fp8 or args.rope or args.max_requests or args.disable_cascade
-                 or args.layers > 1)
+                 or args.layers > 1 or args.prefill_ctas)
     if args.workload == DEFAULT_WORKLOAD and plain and not args.no_workloads:
         extra = {}
         for name in LINE_WORKLOADS:

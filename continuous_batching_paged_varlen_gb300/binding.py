@@ -48,7 +48,8 @@ class Config(ctypes.Structure):
 
 class PlanOptions(ctypes.Structure):
     _fields_ = [("prefill_min_rows", ctypes.c_int32), ("kv_chunk", ctypes.c_int32),
-                ("disable_cascade", ctypes.c_int32), ("target_ctas", ctypes.c_int32)]
+                ("disable_cascade", ctypes.c_int32), ("target_ctas", ctypes.c_int32),
+                ("prefill_ctas", ctypes.c_int32), ("fp8_cache", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -57,7 +58,8 @@ class PlanInfo(ctypes.Structure):
                 ("n_partials", ctypes.c_int32), ("n_cascade_groups", ctypes.c_int32),
                 ("cascade_keys", ctypes.c_int32), ("kv_chunk", ctypes.c_int32),
                 ("total_q", ctypes.c_int32), ("n_launches", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_size_t), ("metadata_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("metadata_bytes", ctypes.c_size_t),
+                ("prefill_ctas", ctypes.c_int32), ("staged_pages", ctypes.c_int32)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -176,8 +178,10 @@ def config(n_q_heads, n_kv_heads, head_dim, page_size, num_pages, max_blocks_per
                   max_blocks_per_req, float(scale or 0.0))
 
 
-def options(prefill_min_rows=0, kv_chunk=0, disable_cascade=0, target_ctas=0) -> PlanOptions:
-    return PlanOptions(prefill_min_rows, kv_chunk, disable_cascade, target_ctas)
+def options(prefill_min_rows=0, kv_chunk=0, disable_cascade=0, target_ctas=0,
+            prefill_ctas=0, fp8_cache=0) -> PlanOptions:
+    return PlanOptions(prefill_min_rows, kv_chunk, disable_cascade, target_ctas, prefill_ctas,
+                       fp8_cache)
 
 
 def _host_i32(a) -> np.ndarray:

@@ -121,7 +121,9 @@ mb_status_t mb_attn_forward_fp8_timed(const mb_plan_t* plan, const void* q,
                                       cudaStream_t stream, cudaEvent_t* events) {
   if (!plan || !plan->workspace) return MB_ERR_INVALID_ARG;
   const PlanDevice& d = plan->dev;
-  if (d.n_prefill_items > 0) return MB_ERR_UNSUPPORTED;
+  // prefill work runs on the tensor-core kernel over bf16 staging pages,
+  // which only a plan built with mb_plan_options_t.fp8_cache has
+  if (d.n_prefill_items > 0 && d.n_stage_pages == 0) return MB_ERR_UNSUPPORTED;
   if (d.total_q == 0) return MB_OK;
   if (!q || !k_codes || !v_codes || !k_scale || !v_scale || !block_table_dev || !out)
     return MB_ERR_INVALID_ARG;
@@ -130,10 +132,61 @@ mb_status_t mb_attn_forward_fp8_timed(const mb_plan_t* plan, const void* q,
       (reinterpret_cast<uintptr_t>(block_table_dev) & 3))
     return MB_ERR_INVALID_ARG;
   uint8_t* ws = static_cast<uint8_t*>(plan->workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  const float scale_log2 = d.scale * kLog2e;
   auto rec = [&](int stage, int which) {
     if (events && events[2 * stage + which]) cudaEventRecord(events[2 * stage + which], stream);
   };
   cudaError_t e = cudaSuccess;
+  const bool overlap = d.n_prefill_items > 0 && d.n_decode_items > 0 && events == nullptr;
+  if (d.n_prefill_items > 0) {
+    // the pages the prefill requests read, dequantized into the workspace's
+    // staging region (laid out like a bf16 cache with staging page ids), then
+    // the bf16 tensor-core prefill over it through the staged block table
+    const size_t half = (size_t)d.n_stage_pages * d.n_kv_heads * d.page_size * d.head_dim * 2;
+    uint8_t* kst = ws + d.off_stage_kv;
+    uint8_t* vst = kst + half;
+    CUtensorMap qm, km, vm;
+    const cuuint64_t kvdims[2] = {(cuuint64_t)d.head_dim,
+                                  (cuuint64_t)d.n_stage_pages * d.n_kv_heads * d.page_size};
+    const cuuint64_t kvstr[1] = {(cuuint64_t)d.head_dim * 2};
+    const cuuint32_t kvbox[2] = {64, (cuuint32_t)d.page_size};
+    const cuuint64_t qdims[3] = {(cuuint64_t)d.head_dim, (cuuint64_t)d.n_q_heads,
+                                 (cuuint64_t)d.total_q};
+    const cuuint64_t qstr[2] = {(cuuint64_t)d.head_dim * 2,
+                                (cuuint64_t)d.n_q_heads * d.head_dim * 2};
+    const cuuint32_t qbox[3] = {64, 1, (cuuint32_t)kPrefillTileM};
+    if (!make_map(&km, kst, 2, kvdims, kvstr, kvbox) ||
+        !make_map(&vm, vst, 2, kvdims, kvstr, kvbox) || !make_map(&qm, q, 3, qdims, qstr, qbox))
+      return MB_ERR_CUDA;
+    rec(MB_STAGE_PREFILL, 0);
+    e = launch_dequant_pages(k_codes, v_codes, k_scale, v_scale,
+                             reinterpret_cast<const int32_t*>(ws + d.off_stage_pages),
+                             d.n_stage_pages, d.n_kv_heads, d.head_dim, d.page_size,
+                             d.num_pages, kst, vst, status, stream);
+    if (e != cudaSuccess) return MB_ERR_CUDA;
+    PrefillArgs a;
+    a.items = reinterpret_cast<const PrefillItem*>(ws + d.off_prefill_items);
+    a.n_items = d.n_prefill_items;
+    a.block_table = reinterpret_cast<const int32_t*>(ws + d.off_stage_bt);
+    a.max_blocks = d.max_blocks;
+    a.n_q_heads = d.n_q_heads;
+    a.n_kv_heads = d.n_kv_heads;
+    a.head_dim = d.head_dim;
+    a.page_size = d.page_size;
+    a.num_pages = d.n_stage_pages;
+    a.scale_log2 = scale_log2;
+    a.out = out;
+    a.lse = lse;
+    a.status = status;
+    a.max_ctas = overlap ? d.prefill_ctas : 0;
+    a.q_map = &qm;
+    a.k_map = &km;
+    a.v_map = &vm;
+    e = launch_prefill(a, stream);
+    rec(MB_STAGE_PREFILL, 1);
+    if (e != cudaSuccess) return MB_ERR_CUDA;
+  }
   if (d.n_decode_items > 0) {
     // K codes as rows of head_dim bytes, one page of one KV head per box,
     // swizzled into the K-major operand layout of the e4m3 MMA
@@ -162,16 +215,19 @@ mb_status_t mb_attn_forward_fp8_timed(const mb_plan_t* plan, const void* q,
     a.head_dim = d.head_dim;
     a.page_size = d.page_size;
     a.num_pages = d.num_pages;
-    a.scale_log2 = d.scale * kLog2e;
+    a.scale_log2 = scale_log2;
     a.out = out;
     a.lse = lse;
     a.part_o = reinterpret_cast<float*>(ws + d.off_part_o);
     a.part_lse = reinterpret_cast<float*>(ws + d.off_part_lse);
     a.row_merge = reinterpret_cast<const MergeRef*>(ws + d.off_row_merge);
     a.combine_count = d.n_combine > 0 ? reinterpret_cast<int32_t*>(ws + d.off_combine_count) : nullptr;
-    a.status = reinterpret_cast<int32_t*>(ws);
+    a.status = status;
+    a.after_prefill = d.n_prefill_items > 0 ? 1 : 0;
+    a.done_counter = reinterpret_cast<int32_t*>(ws + kDoneCounterOffset);
     rec(MB_STAGE_DECODE, 0);
-    e = launch_decode_fp8(a, stream);
+    // behind the prefill kernel, on the SMs its grid leaves free
+    e = launch_decode_fp8(a, stream, overlap);
     rec(MB_STAGE_DECODE, 1);
     if (e != cudaSuccess) return MB_ERR_CUDA;
   }
@@ -262,13 +318,13 @@ mb_status_t mb_attn_forward_timed(const mb_plan_t* plan, const void* q, const vo
         !make_map(&vm, v_cache, 2, kvdims, kvstr, kvbox))
       return MB_ERR_CUDA;
   }
-  // With both kinds of work the prefill kernel goes first and the split-KV
-  // kernel is launched to overlap it (programmatic stream serialization):
-  // it starts once every prefill CTA has been dispatched and fills the SMs
-  // the prefill's heaviest-first queue leaves idle at its end. The combine
-  // kernel is ordered after both.
-  // (The timed variant launches back to back so that each stage's events
-  // bracket that stage alone.)
+  // With both kinds of work the prefill kernel goes first, its persistent
+  // grid on the plan's share of the SMs, and the split-KV kernel is launched
+  // to overlap it (programmatic stream serialization): it starts once every
+  // prefill CTA has been dispatched, streams its key ranges on the SMs the
+  // prefill leaves free and spreads over the rest as the prefill CTAs
+  // finish. (The timed variant launches back to back, each kernel on the
+  // whole GPU, so that each stage's events bracket that stage alone.)
   const bool overlap = d.n_prefill_items > 0 && d.n_decode_items > 0 && events == nullptr;
   if (d.n_prefill_items > 0) {
     const cuuint64_t qdims[3] = {(cuuint64_t)d.head_dim, (cuuint64_t)d.n_q_heads,
@@ -291,6 +347,7 @@ mb_status_t mb_attn_forward_timed(const mb_plan_t* plan, const void* q, const vo
     a.out = out;
     a.lse = lse;
     a.status = status;
+    a.max_ctas = overlap ? d.prefill_ctas : 0;
     a.q_map = &qm;
     a.k_map = &km;
     a.v_map = &vm;
@@ -322,10 +379,14 @@ mb_status_t mb_attn_forward_timed(const mb_plan_t* plan, const void* q, const vo
     a.row_merge = reinterpret_cast<const MergeRef*>(ws + d.off_row_merge);
     a.combine_count = d.n_combine > 0 ? reinterpret_cast<int32_t*>(ws + d.off_combine_count) : nullptr;
     a.status = status;
+    a.after_prefill = d.n_prefill_items > 0 ? 1 : 0;
+    a.done_counter = reinterpret_cast<int32_t*>(ws + kDoneCounterOffset);
     a.k_map = &km;
     a.v_map = &vm;
     rec(MB_STAGE_DECODE, 0);
-    e = launch_decode(a, stream, overlap);
+    // behind the prefill kernel (overlap) or behind whatever came before
+    // (the append, whose tail the kernel's history streaming then overlaps)
+    e = launch_decode(a, stream, events == nullptr);
     rec(MB_STAGE_DECODE, 1);
     if (e != cudaSuccess) return MB_ERR_CUDA;
   }

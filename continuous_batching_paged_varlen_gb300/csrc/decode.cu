@@ -59,10 +59,14 @@ enum {
   B_KV_FULL = 0,              // + slot
   B_KV_EMPTY = kSlots,        // + slot
   B_S_FULL = 2 * kSlots,      // + buffer
-  B_P_FULL = 2 * kSlots + 2,
-  B_O_DONE = 2 * kSlots + 3,
-  B_VZ_READY = 2 * kSlots + 4,
-  B_COUNT = 2 * kSlots + 5
+  // P(j) written / P(j) V(j) done, one barrier per tile parity: the softmax
+  // warps may run a tile ahead of the PV that reads their P, so a single
+  // barrier could complete twice before its waiter looks (parity waits
+  // cannot tell those apart); per parity, no waiter falls two phases behind
+  B_P_FULL = 2 * kSlots + 2,  // + (j & 1)
+  B_O_DONE = 2 * kSlots + 4,  // + (j & 1)
+  B_VZ_READY = 2 * kSlots + 6,
+  B_COUNT = 2 * kSlots + 7
 };
 
 template <int D>
@@ -103,6 +107,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* merge_n = reinterpret_cast<int*>(smem + L::misc_off + 8);
   int4* merge_list = reinterpret_cast<int4*>(sq);
 
+  // the kernel behind this one (the next layer's append, say) may launch now
+  pdl_launch_dependents();
+  const bool dep_wait = a.after_prefill == 0;
   const DecodeItem it = a.items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nr = it.n_rows;
@@ -117,8 +124,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars[B_S_FULL + 0], 1);
     mbar_init(&bars[B_S_FULL + 1], 1);
-    mbar_init(&bars[B_P_FULL], active_warps);
-    mbar_init(&bars[B_O_DONE], 1);
+    mbar_init(&bars[B_P_FULL + 0], active_warps);
+    mbar_init(&bars[B_P_FULL + 1], active_warps);
+    mbar_init(&bars[B_O_DONE + 0], 1);
+    mbar_init(&bars[B_O_DONE + 1], 1);
     mbar_init(&bars[B_VZ_READY], 1);
     *abort_flag = 0;
     *merge_n = 0;
@@ -146,6 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // gather the item's query rows into the K-major 128-byte-swizzled Q tile
     // (rows past n_rows are zero): warps 0-3 and 5, every load in flight
     // before the producer is released, then the stores
+    // q may be the kernel ahead's output (a rotary append rewrites it)
+    if (dep_wait) pdl_wait();
     const uint4* q = static_cast<const uint4*>(a.q);
     constexpr int CH = D / 8;  // 16-byte chunks per row
     constexpr int kGather = kThreads - 32;
@@ -185,19 +196,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int npg = BN / ps, nbox = npg * L::kHalves;
     const int my_pg = lane % npg, my_h2 = lane / npg;
     int32_t my_y = 0;
+    int32_t page_next = page0;  // keys past k_end map to the last page: masked, V zeroed
     int issued = 0;
+    // dep_wait: history keys were written before the kernel ahead ran, so
+    // the ring fills with them at once; the wait for that kernel comes at the
+    // first tile that reaches this step's new rows, or before the first slot
+    // is reused (so no bounded wait below runs while the kernel ahead does).
+    // Then, as without dep_wait after K_0, the producer lets the Q loads
+    // (issued by the other warps right after their own wait) go first.
+    bool waited = !dep_wait, q_first = false;
     for (int i = 0; i < 2 * n; ++i) {
       const int j = i >> 1, slot = i % kSlots;
       const uint32_t ph = (uint32_t)(i / kSlots) & 1u;
-      if (i == 1) named_barrier_sync(2, kThreads);  // every Q load issued (n >= 1)
+      if (!waited && (i >= kSlots || it.k_begin + (j + 1) * BN > it.k_new)) {
+        pdl_wait();
+        waited = true;
+      }
+      if (!q_first && waited && (dep_wait || i == 1)) {
+        named_barrier_sync(2, kThreads);  // every Q load issued
+        q_first = true;
+      }
       if (i >= kSlots &&
           !__all_sync(0xffffffffu, mbar_wait(&bars[B_KV_EMPTY + slot], ph ^ 1u, abort_flag,
                                              a.status)))
         break;
       if ((i & 1) == 0 && lane < npg) {
-        int b = first_block + j * npg + lane;
-        if (b > last_block) b = last_block;  // keys past k_end: masked, V zeroed
-        int32_t page = j == 0 ? page0 : __ldg(btrow + b);
+        // this lane's page of K_j / V_j, loaded one K tile ahead: the load's
+        // latency then overlaps the waits and copies of the tile before it
+        // (a dependent load here would stall every refill of the ring)
+        int32_t page = page_next;
+        if (j + 1 < n)
+          page_next = __ldg(btrow + min(first_block + (j + 1) * npg + lane, last_block));
         if ((unsigned)page >= (unsigned)a.num_pages) {
           set_status(a.status, MB_ERR_DEVICE_INDEX);
           page = 0;
@@ -240,6 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0)
       for (int i = max(0, issued - kSlots); i < issued; ++i)
         mbar_drain(&bars[B_KV_FULL + i % kSlots], (uint32_t)(i / kSlots) & 1u, kDrainNs);
+    // this warp also writes merged rows below
+    if (!waited) pdl_wait();
+    if (!q_first && n > 0) named_barrier_sync(2, kThreads);
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -273,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int vi = 2 * j + 1;
         if (!(ok = wait(B_KV_FULL + vi % kSlots, (uint32_t)(vi / kSlots) & 1u))) break;
         if (j == n - 1 && tail_zero && !(ok = wait(B_VZ_READY, 0))) break;
-        if (!(ok = wait(B_P_FULL, (uint32_t)j & 1u))) break;
+        if (!(ok = wait(B_P_FULL + (j & 1), (uint32_t)(j >> 1) & 1u))) break;
         const uint32_t v0 = kva + (vi % kSlots) * L::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
@@ -281,13 +313,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_bf16_ts(tmem + kColO, tmem + kColS + 128 * (j & 1) + kk * 8, bd, idesc_pv,
                        (j > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&bars[B_O_DONE]);
+        umma_commit(&bars[B_O_DONE + (j & 1)]);
         umma_commit(&bars[B_KV_EMPTY + vi % kSlots]);
         last_pv = j;
         // S(j+2) reuses this buffer; it follows PV(j) in issue order
         if (j + 2 < n && !(ok = issue_s(j + 2))) break;
       }
-      if (last_pv >= 0) mbar_drain(&bars[B_O_DONE], (uint32_t)last_pv & 1u, kDrainNs);
+      if (last_pv >= 0)
+        mbar_drain(&bars[B_O_DONE + (last_pv & 1)], (uint32_t)(last_pv >> 1) & 1u, kDrainNs);
     }
   } else if (warp < active_warps) {
     // ------------------------------------------------------------ softmax
@@ -356,13 +389,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk[e >> 1] = pack_bf16x2(e0, e1);
       }
       l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
-      if (j > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE], (uint32_t)(j - 1) & 1u,
+      // P(j) goes over S(j) in buffer j & 1, which PV(j - 2) read last: S(j)
+      // was issued after PV(j - 2), so that PV is done. Only a rescale of O
+      // must wait for PV(j - 1), which accumulates into O (the only PV that
+      // can still run: PV(j) needs this P). So the PV's latency stays off
+      // the per-tile chain unless a row's max grew by more than 2^8.
+      if (__any_sync(0xffffffffu, need)) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + ((j - 1) & 1)],
+                                               (uint32_t)((j - 1) >> 1) & 1u,
                                                abort_flag, a.status));
         if (!ok) break;
-      }
-      tc_fence_after();
-      if (__any_sync(0xffffffffu, need)) {
+        tc_fence_after();
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
@@ -378,10 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_P_FULL]);
+      if (lane == 0) mbar_arrive(&bars[B_P_FULL + (j & 1)]);
     }
     if (ok && n > 0)
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE], (uint32_t)(n - 1) & 1u,
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + ((n - 1) & 1)],
+                                             (uint32_t)((n - 1) >> 1) & 1u,
                                              abort_flag, a.status));
     if (ok && n > 0) {
       tc_fence_after();
@@ -445,6 +483,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __threadfence();
     dev::merge_listed_rows<D, kThreads>(merge_list, nl, a.part_o, a.part_lse,
                                         static_cast<__nv_bfloat16*>(a.out), a.lse);
+  }
+  if (!dep_wait && threadIdx.x == 0) {
+    // started under the prefill kernel's tail: the grid must not complete
+    // before that kernel does (what follows on the stream counts on it), so
+    // the last CTA to finish waits for it
+    __threadfence();
+    if (atomicAdd(a.done_counter, 1) == (int)gridDim.x - 1) {
+      pdl_wait();
+      atomicExch(a.done_counter, 0);
+    }
   }
 }
 

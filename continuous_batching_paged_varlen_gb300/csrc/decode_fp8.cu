@@ -144,22 +144,11 @@ __device__ __forceinline__ SeqItem seq_item(int s, int n) {
   return {m - 1, true};
 }
 
-// Two e4m3 codes (low byte first) -> f16x2 (exact).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((unsigned short)(two & 0xffffu)));
-  return r;
-}
 // (lo, hi) fp32 -> two e4m3 codes (lo in the low byte), nearest, saturating.
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
   unsigned short r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
-}
-__device__ __forceinline__ void f16x2_to_f32x2(uint32_t h, float& lo, float& hi) {
-  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-      : "=f"(lo), "=f"(hi)
-      : "r"(h));
 }
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
@@ -605,6 +594,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
 
+  // the kernel behind this one (the next layer's append, say) may launch now
+  pdl_launch_dependents();
   const DecodeItem it = a.items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nr = it.n_rows;
@@ -931,11 +922,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the K ring is no longer written (every copy has landed) nor read
     dev::merge_completed_rows<D, kThreads>(mg, reinterpret_cast<uint32_t*>(sk));
   }
+  if (a.after_prefill && threadIdx.x == 0) {
+    // started under the prefill kernel's tail: the grid must not complete
+    // before that kernel does, so the last CTA to finish waits for it
+    __threadfence();
+    if (atomicAdd(a.done_counter, 1) == (int)gridDim.x - 1) {
+      pdl_wait();
+      atomicExch(a.done_counter, 0);
+    }
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_decode_fp8(const DecodeFp8Args& a, cudaStream_t s) {
+cudaError_t launch_decode_fp8(const DecodeFp8Args& a, cudaStream_t s, bool overlap_previous) {
   if (a.n_items <= 0) return cudaSuccess;
   const int ps_shift = __builtin_ctz((unsigned)a.page_size);
   static OncePerDevice setup128, setup64;
@@ -947,6 +947,9 @@ cudaError_t launch_decode_fp8(const DecodeFp8Args& a, cudaStream_t s) {
                                   (int)Layout<128>::kAlloc);
     });
     if (e != cudaSuccess) return e;
+    if (overlap_previous)
+      return launch_programmatic(splitkv_fp8_kernel<128>, dim3((unsigned)a.n_items),
+                                 dim3(kThreads), Layout<128>::kAlloc, s, a, ps_shift, *a.k_map);
     splitkv_fp8_kernel<128><<<(unsigned)a.n_items, kThreads, Layout<128>::kAlloc, s>>>(
         a, ps_shift, *a.k_map);
     return cudaGetLastError();
@@ -957,6 +960,9 @@ cudaError_t launch_decode_fp8(const DecodeFp8Args& a, cudaStream_t s) {
                                 (int)Layout<64>::kAlloc);
   });
   if (e != cudaSuccess) return e;
+  if (overlap_previous)
+    return launch_programmatic(splitkv_fp8_kernel<64>, dim3((unsigned)a.n_items),
+                               dim3(kThreads), Layout<64>::kAlloc, s, a, ps_shift, *a.k_map);
   splitkv_fp8_kernel<64><<<(unsigned)a.n_items, kThreads, Layout<64>::kAlloc, s>>>(
       a, ps_shift, *a.k_map);
   return cudaGetLastError();

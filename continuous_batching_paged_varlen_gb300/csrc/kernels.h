@@ -41,6 +41,14 @@ cudaError_t launch_kv_append_fp8(void* k8, void* v8, float* ks, float* vs, const
                                  int32_t n_kv_heads, int32_t head_dim, int32_t page_size,
                                  int32_t num_pages, int32_t* status, cudaStream_t s);
 
+// fp8 cache pages -> bf16 staging pages for the prefill kernel (kv_append.cu):
+// staged page i (cache page stage_pages[i]) of every KV head, K and V.
+cudaError_t launch_dequant_pages(const void* k8, const void* v8, const float* ks,
+                                 const float* vs, const int32_t* stage_pages, int32_t n_stage,
+                                 int32_t n_kv_heads, int32_t head_dim, int32_t page_size,
+                                 int32_t num_pages, void* k_stage, void* v_stage,
+                                 int32_t* status, cudaStream_t s);
+
 // Fused rotary embedding + KV append (rope_append.cu).
 cudaError_t launch_rope_append(void* q, void* k_cache, void* v_cache, const void* k_new,
                                const void* v_new, const int32_t* positions,
@@ -70,12 +78,20 @@ struct DecodeArgs {
   const MergeRef* row_merge;
   int32_t* combine_count;
   int32_t* status;
+  // 1: the kernel ahead on the stream is the same forward's prefill kernel,
+  // which writes nothing this kernel reads: no wait before the work, and the
+  // last CTA to finish waits for that kernel (counted in done_counter), so
+  // this grid completes after it. 0: the kernel ahead may have written q,
+  // this step's K/V rows or the outputs: Q, keys >= an item's k_new and
+  // every global write wait for it; history keys stream at once.
+  int32_t after_prefill;
+  int32_t* done_counter;
   const CUtensorMap* k_map;  // host copies, passed by value to the kernel
   const CUtensorMap* v_map;
 };
 // overlap_previous: launch with programmatic stream serialization, so the
-// kernel may start while the previous kernel on the stream (which must not
-// produce anything it reads) is still running.
+// kernel may start while the previous kernel on the stream is running (the
+// waits above keep it correct).
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, bool overlap_previous = false);
 
 // Split-KV / cascade kernel over an fp8 (e4m3) cache with per-row fp32
@@ -99,9 +115,11 @@ struct DecodeFp8Args {
   const MergeRef* row_merge;  // as in DecodeArgs
   int32_t* combine_count;
   int32_t* status;
+  int32_t after_prefill;      // as in DecodeArgs (the fp8 kernel is launched
+  int32_t* done_counter;      // behind the prefill only, never behind an append)
   const CUtensorMap* k_map;  // uint8 codes [rows, D], box D x ps, swizzled (host copy)
 };
-cudaError_t launch_decode_fp8(const DecodeFp8Args& a, cudaStream_t s);
+cudaError_t launch_decode_fp8(const DecodeFp8Args& a, cudaStream_t s, bool overlap_previous = false);
 
 // tcgen05 prefill kernel (prefill.cu).
 struct PrefillArgs {
@@ -113,6 +131,7 @@ struct PrefillArgs {
   void* out;
   float* lse;
   int32_t* status;
+  int32_t max_ctas;          // persistent grid cap (0: one CTA per SM)
   const CUtensorMap* q_map;  // host copies, passed by value to the kernel
   const CUtensorMap* k_map;
   const CUtensorMap* v_map;

@@ -9,6 +9,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "../../include/mb.h"
@@ -28,6 +29,18 @@ __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two e4m3 codes (low byte first) -> f16x2 (exact: every e4m3 value is an f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((unsigned short)(two & 0xffffu)));
+  return r;
+}
+__device__ __forceinline__ void f16x2_to_f32x2(uint32_t h, float& lo, float& hi) {
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h));
 }
 
 // 2^x on the MUFU unit (PTX ex2.approx.ftz.f32); 2^-inf = +0.
@@ -73,6 +86,17 @@ __device__ __forceinline__ uint64_t globaltimer() {
 
 __device__ __forceinline__ void set_status(int32_t* status, int code) {
   if (status) atomicOr(status, 1 << code);
+}
+
+// ---------------------------------------------------------------- launch order
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the kernel before it on the stream is still
+// running: pdl_wait blocks the calling thread until every grid it depends on
+// has completed and its writes are visible (at once when there is none), and
+// pdl_launch_dependents lets the kernel after this one start early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- mbarrier
@@ -409,4 +433,24 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_maj
 }
 
 }  // namespace dev
+
+// Host: launch `kernel` with programmatic stream serialization, so that it
+// may start before the previous kernel on `stream` has finished (the kernel
+// itself calls dev::pdl_wait before it touches what that kernel may write).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_programmatic(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 }  // namespace mb

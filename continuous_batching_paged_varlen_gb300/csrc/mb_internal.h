@@ -10,9 +10,18 @@
 //   rows                RowDesc[n_decode_rows]        (query rows of those CTAs)
 //   prefill_items       PrefillItem[n_prefill_items]  (tensor-core prefill CTAs)
 //   combine             CombineEntry[n_combine]       (rows merged from partials)
+//   row_merge           MergeRef[n_decode_rows]       (per row: its merge reference)
+//   combine_count       int32[n_combine]              (arrival counters, zero)
+//   stage_pages         int32[n_stage_pages]          (fp8 plans: cache pages the
+//                                                      prefill reads, staged)
+//   stage_bt            int32[n_reqs * max_blocks]    (fp8 plans: the prefill
+//                                                      requests' block tables
+//                                                      in staging page ids)
 //   ---- metadata above is uploaded; scratch below is written by kernels ----
 //   part_lse            float[n_partials]             (log2-domain LSE per partial)
 //   part_o              float[n_partials * head_dim]  (normalised partial outputs)
+//   stage_kv            bf16 K then V [n_stage_pages, n_kv_heads, page_size,
+//                       head_dim] (fp8 plans: the staged pages, dequantized)
 #pragma once
 
 #include <stdint.h>
@@ -20,6 +29,10 @@
 namespace mb {
 
 constexpr int kStatusBytes = 256;
+// int32 at this workspace offset (inside the status region, zero in the
+// uploaded image): CTAs of a split-KV launch that finished, counted by the
+// kernel launched behind the prefill kernel; its last CTA puts it back to zero
+constexpr int kDoneCounterOffset = 4;
 constexpr int kRowsPerDecodeItem = 128; // query rows one split-KV CTA owns (TMEM lanes)
 constexpr int kPrefillTileM = 128;      // query rows per prefill tile (one TMEM accumulator)
 constexpr int kPrefillTileN = 128;      // keys per prefill KV tile
@@ -34,7 +47,8 @@ struct DecodeItem {
   int32_t k_end;
   int32_t row_begin;  // first RowDesc
   int32_t n_rows;     // <= kRowsPerDecodeItem
-  int32_t pad0, pad1;
+  int32_t k_new;      // keys >= k_new may hold this step's appended rows (k_end: none)
+  int32_t pad1;
 };
 
 struct RowDesc {
@@ -84,9 +98,12 @@ struct PlanDevice {
   int32_t n_decode_items, n_decode_rows, n_prefill_items, n_combine, n_partials;
   int32_t n_q_heads, n_kv_heads, head_dim, page_size, num_pages, max_blocks;
   int32_t total_q;
+  int32_t prefill_ctas;  // prefill grid when the split-KV kernel runs beside it
   float scale;
   size_t off_decode_items, off_rows, off_prefill_items, off_combine, off_row_merge,
       off_combine_count, off_part_lse, off_part_o;
+  int32_t n_stage_pages;  // fp8 plans with prefill work: pages staged as bf16
+  size_t off_stage_pages, off_stage_bt, off_stage_kv;
   size_t metadata_bytes, workspace_bytes;
 };
 

@@ -185,6 +185,8 @@ extern "C" mb_status_t mb_attn_forward_noalloc(const mb_plan_t* plan, const void
     a.row_merge = reinterpret_cast<const MergeRef*>(ws + d.off_row_merge);
     a.combine_count = d.n_combine > 0 ? reinterpret_cast<int32_t*>(ws + d.off_combine_count) : nullptr;
     a.status = status;
+    a.after_prefill = 0;
+    a.done_counter = reinterpret_cast<int32_t*>(ws + kDoneCounterOffset);
     a.k_map = &km;
     a.v_map = &vm;
     if (launch_decode(a, stream) != cudaSuccess) return MB_ERR_CUDA;
@@ -211,6 +213,7 @@ extern "C" mb_status_t mb_attn_forward_noalloc(const mb_plan_t* plan, const void
     a.out = out;
     a.lse = lse;
     a.status = status;
+    a.max_ctas = 0;
     a.q_map = &qm;
     a.k_map = &km;
     a.v_map = &vm;

@@ -38,6 +38,20 @@ constexpr int kMinChunk = 1024;
 constexpr int64_t kSmallBatchTiles = (int64_t)kSms * 8;
 constexpr int kMinSmallChunk = 256;
 
+// Cost model of a mixed iteration (both kernels), measured on a GB300 at the
+// maximum SM clock: one 128-key tile of one 128-row query tile on the
+// tensor-core prefill kernel (D = 128; the issue-bound kernel runs D / 16 + 8
+// MMAs per tile), a prefill work item's fixed cost, the rate at which one SM
+// of the split-KV kernel streams K/V when HBM is not the limit, and the HBM
+// rate the split-KV kernel reaches on the whole GPU.
+constexpr double kPrefillTileUs = 0.85;
+constexpr double kPrefillItemUs = 2.0;
+constexpr double kDecodeSmGBs = 65.0;
+constexpr double kHbmGBs = 6600.0;
+// the same two rates for the split-KV kernel over an fp8 cache
+constexpr double kDecodeFp8SmGBs = 26.0;
+constexpr double kHbmFp8GBs = 3950.0;
+
 bool is_pow2_in(int v, int lo, int hi) {
   return v >= lo && v <= hi && (v & (v - 1)) == 0;
 }
@@ -126,6 +140,61 @@ std::vector<int32_t> heavy_first(size_t n, KeyFn key) {
   return order;
 }
 
+// SMs for the persistent prefill grid when the split-KV kernel runs beside
+// it: the grid P whose modelled step time is least (the largest such P on a
+// tie). The prefill items (heavy first) go to P CTAs in snake order, which
+// gives each CTA its finishing time. Over time the split-KV kernel has the
+// kSms - P SMs without a prefill CTA, plus every prefill SM whose CTA has
+// finished (its CTAs are handed out as SMs free up); it streams at sm_gbs
+// per SM, never faster than full_gbs. The step ends when both are done.
+int32_t partition_sms(const std::vector<PrefillItem>& pitems, int64_t decode_bytes, int D,
+                      double sm_gbs, double full_gbs) {
+  const int32_t n = (int32_t)pitems.size();
+  const int32_t hi = std::min<int32_t>(n, kSms);
+  const double tile_us = kPrefillTileUs * (D / 16 + 8) / 16.0;
+  std::vector<double> cost((size_t)n);
+  for (int32_t i = 0; i < n; ++i) {
+    const PrefillItem& p = pitems[(size_t)i];
+    const int32_t ra = std::min(kPrefillTileM, p.n_rows), rb = std::max(0, p.n_rows - kPrefillTileM);
+    const int32_t na = (std::min(p.kv_length, p.s0 + p.i0 + ra) + kPrefillTileN - 1) / kPrefillTileN;
+    const int32_t nb = rb > 0 ? (std::min(p.kv_length, p.s0 + p.i0 + kPrefillTileM + rb) +
+                                 kPrefillTileN - 1) / kPrefillTileN
+                              : 0;
+    cost[(size_t)i] = kPrefillItemUs + (na + nb) * tile_us;
+  }
+  const double bytes_per_us_sm = sm_gbs * 1e3, bytes_per_us_full = full_gbs * 1e3;
+  int32_t best = hi;
+  double best_t = 1e300;
+  std::vector<double> load;
+  for (int32_t P = hi; P >= std::max<int32_t>(1, hi / 4); --P) {
+    load.assign((size_t)P, 0.0);
+    for (int32_t k = 0; k * P < n; ++k)
+      for (int32_t b = 0; b < P; ++b) {
+        const int32_t idx = k * P + ((k & 1) ? P - 1 - b : b);
+        if (idx < n) load[(size_t)b] += cost[(size_t)idx];
+      }
+    std::sort(load.begin(), load.end());
+    const double t_pre = load.back();
+    // walk the intervals between prefill CTAs' finishing times
+    double left = (double)decode_bytes, t = 0.0, t_dec = -1.0;
+    int32_t free_sms = kSms - P;
+    for (int32_t b = 0; b <= P && t_dec < 0.0; ++b) {
+      const double t_next = b < P ? load[(size_t)b] : 1e300;
+      const double rate = std::min(bytes_per_us_full, free_sms * bytes_per_us_sm);
+      if (rate > 0.0 && left <= rate * (t_next - t)) t_dec = t + left / rate;
+      else if (rate > 0.0) left -= rate * (t_next - t);
+      t = t_next;
+      ++free_sms;
+    }
+    const double step = std::max(t_pre, t_dec);
+    if (step < best_t * (1.0 - 1e-3)) {
+      best_t = step;
+      best = P;
+    }
+  }
+  return best;
+}
+
 }  // namespace
 
 mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
@@ -141,6 +210,7 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
   if (opts) o = *opts;
   if (o.kv_chunk < 0 || (o.kv_chunk % 64) != 0 || o.target_ctas < 0)
     return MB_ERR_INVALID_ARG;
+  if (o.prefill_ctas > kSms) o.prefill_ctas = kSms;
   const int prefill_min = o.prefill_min_rows == 0 ? kDefaultPrefillMinRows
                                                   : o.prefill_min_rows;
   const int target = o.target_ctas ? o.target_ctas : kDefaultTargetCtas;
@@ -358,6 +428,12 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
         it.kv_head = h;
         it.k_begin = kb;
         it.k_end = ke;
+        // a shared prefix lies below every sharer's new rows; a request's own
+        // range holds its new rows from S0 on
+        it.k_new = s.shared ? ke
+                            : std::min(ke, std::max(kb, reqs[s.bt_row].kv_length -
+                                                            (reqs[s.bt_row].q_end -
+                                                             reqs[s.bt_row].q_start)));
         it.row_begin = (int32_t)rows.size();
         for (int32_t x = s.mbeg; x < s.mend; ++x) {
           const int32_t r = member_list[x];
@@ -427,6 +503,44 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
     pitems.swap(sorted);
   }
 
+  // ---- SMs of the prefill grid beside the split-KV kernel ---------------
+  int32_t prefill_ctas = std::min<int32_t>((int32_t)pitems.size(), kSms);
+  if (!pitems.empty() && !items.empty()) {
+    if (o.prefill_ctas > 0) {
+      prefill_ctas = std::min(prefill_ctas, o.prefill_ctas);
+    } else if (o.prefill_ctas == 0) {
+      // K and V bytes the split-KV CTAs read (fp8: codes and row scales)
+      const int64_t per_key = o.fp8_cache ? 2 * (D + 4) : 4 * D;
+      int64_t dbytes = 0;
+      for (const DecodeItem& it : items) dbytes += (int64_t)(it.k_end - it.k_begin) * per_key;
+      prefill_ctas = o.fp8_cache
+                         ? partition_sms(pitems, dbytes, D, kDecodeFp8SmGBs, kHbmFp8GBs)
+                         : partition_sms(pitems, dbytes, D, kDecodeSmGBs, kHbmGBs);
+    }
+  }
+
+  // ---- fp8 cache: pages of the prefill requests, staged as bf16 ----------
+  // the prefill kernel reads them through stage_bt, a copy of the block
+  // table whose prefill rows hold staging page ids; a page several prefill
+  // requests map is staged once
+  std::vector<int32_t> stage_pages;
+  std::vector<int32_t> stage_bt;
+  if (o.fp8_cache && !pitems.empty()) {
+    std::vector<int32_t> stage_of((size_t)cfg->num_pages, -1);
+    stage_bt.assign((size_t)n * mb, 0);
+    for (int32_t r : prefill_reqs) {
+      const int32_t nb = (reqs[r].kv_length + ps - 1) / ps;
+      for (int32_t b = 0; b < nb; ++b) {
+        const int32_t page = bt[(size_t)r * mb + b];
+        if (stage_of[(size_t)page] < 0) {
+          stage_of[(size_t)page] = (int32_t)stage_pages.size();
+          stage_pages.push_back(page);
+        }
+        stage_bt[(size_t)r * mb + b] = stage_of[(size_t)page];
+      }
+    }
+  }
+
   // ---- workspace layout + host image -----------------------------------
   PlanDevice& d = plan->dev;
   d = PlanDevice{};
@@ -442,6 +556,7 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
   d.num_pages = cfg->num_pages;
   d.max_blocks = mb;
   d.total_q = total_q;
+  d.prefill_ctas = pitems.empty() ? 0 : prefill_ctas;
   d.scale = cfg->scale > 0.f ? cfg->scale : 1.0f / sqrtf((float)D);
   size_t off = kStatusBytes;
   d.off_decode_items = off;
@@ -459,11 +574,18 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
   off = align256(off + rows.size() * sizeof(MergeRef));
   d.off_combine_count = off;
   off = align256(off + combine.size() * sizeof(int32_t));
+  d.n_stage_pages = (int32_t)stage_pages.size();
+  d.off_stage_pages = off;
+  off = align256(off + stage_pages.size() * sizeof(int32_t));
+  d.off_stage_bt = off;
+  off = align256(off + stage_bt.size() * sizeof(int32_t));
   d.metadata_bytes = off;
   d.off_part_lse = off;
   off = align256(off + (size_t)n_partials * sizeof(float));
   d.off_part_o = off;
   off = align256(off + (size_t)n_partials * D * sizeof(float));
+  d.off_stage_kv = off;
+  off = align256(off + 2 * stage_pages.size() * (size_t)Hkv * ps * D * 2);
   d.workspace_bytes = off;
 
   plan->host_image.assign(d.metadata_bytes, 0);
@@ -475,6 +597,10 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
     memcpy(img + d.off_prefill_items, pitems.data(), pitems.size() * sizeof(PrefillItem));
   if (!combine.empty())
     memcpy(img + d.off_combine, combine.data(), combine.size() * sizeof(CombineEntry));
+  if (!stage_pages.empty()) {
+    memcpy(img + d.off_stage_pages, stage_pages.data(), stage_pages.size() * sizeof(int32_t));
+    memcpy(img + d.off_stage_bt, stage_bt.data(), stage_bt.size() * sizeof(int32_t));
+  }
   {
     std::vector<int32_t> slot_entry((size_t)n_partials, -1);
     for (size_t e = 0; e < combine.size(); ++e)
@@ -507,6 +633,8 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
   info.n_launches = (d.n_decode_items > 0) + (d.n_prefill_items > 0);
   info.workspace_bytes = d.workspace_bytes;
   info.metadata_bytes = d.metadata_bytes;
+  info.prefill_ctas = d.prefill_ctas;
+  info.staged_pages = d.n_stage_pages;
   return MB_OK;
 }
 

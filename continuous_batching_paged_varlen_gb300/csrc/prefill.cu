@@ -632,6 +632,7 @@ cudaError_t launch_d(const PrefillArgs& a, cudaStream_t s) {
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
   }
+  if (a.max_ctas > 0 && a.max_ctas < sms) sms = a.max_ctas;
   const int grid = a.n_items < sms ? a.n_items : sms;
   prefill_kernel<D><<<grid, kThreads, smem, s>>>(p, *a.q_map, *a.k_map, *a.v_map);
   return cudaGetLastError();

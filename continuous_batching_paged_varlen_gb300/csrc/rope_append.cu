@@ -51,6 +51,10 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(
   constexpr int HALF = D / 2;
   constexpr int RU = D / 16;  // rotation units per row: 8 elements of each half
   constexpr int CH = D / 8;   // 16-byte chunks per row
+  // nothing here runs before the kernel ahead (which may read the cache or
+  // q, or write k_new) is done
+  dev::pdl_launch_dependents();
+  dev::pdl_wait();
   const int t = blockIdx.x;
   const int32_t pos = __ldg(positions + t);
   if (pos < 0 || pos >= max_position) {
@@ -118,17 +122,12 @@ cudaError_t launch_rope_append(void* q, void* k_cache, void* v_cache, const void
                                int32_t* status, cudaStream_t s) {
   const int ps_shift = __builtin_ctz((unsigned)page_size);
   const int64_t n_slots = (int64_t)num_pages * page_size;
-  if (head_dim == 128)
-    rope_append_kernel<128><<<(unsigned)T, kThreads, 0, s>>>(
-        (__nv_bfloat16*)q, (__nv_bfloat16*)k_cache, (uint4*)v_cache,
-        (const __nv_bfloat16*)k_new, (const uint4*)v_new, positions, slots, n_q_heads,
-        n_kv_heads, ps_shift, n_slots, cos_sin, max_position, status);
-  else
-    rope_append_kernel<64><<<(unsigned)T, kThreads, 0, s>>>(
-        (__nv_bfloat16*)q, (__nv_bfloat16*)k_cache, (uint4*)v_cache,
-        (const __nv_bfloat16*)k_new, (const uint4*)v_new, positions, slots, n_q_heads,
-        n_kv_heads, ps_shift, n_slots, cos_sin, max_position, status);
-  return cudaGetLastError();
+  return launch_programmatic(head_dim == 128 ? rope_append_kernel<128> : rope_append_kernel<64>,
+                             dim3((unsigned)T), dim3(kThreads), 0, s, (__nv_bfloat16*)q,
+                             (__nv_bfloat16*)k_cache, (uint4*)v_cache,
+                             (const __nv_bfloat16*)k_new, (const uint4*)v_new, positions, slots,
+                             n_q_heads, n_kv_heads, ps_shift, n_slots, cos_sin, max_position,
+                             status);
 }
 
 }  // namespace mb

@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define MB_ABI_VERSION 1
+#define MB_ABI_VERSION 2
 
 typedef enum {
   MB_OK = 0,
@@ -106,6 +106,15 @@ typedef struct {
                                 0 -> chosen from the batch (>= 1024)         */
   int32_t disable_cascade;   /* 1 -> no shared-prefix grouping               */
   int32_t target_ctas;       /* split-KV work items to aim for; 0 -> auto     */
+  int32_t prefill_ctas;      /* when a plan holds both kinds of work, the SMs
+                                the persistent prefill grid takes while the
+                                split-KV kernel streams on the rest (one CTA
+                                per SM each); 0 -> chosen by the planner's
+                                cost model; < 0 -> every SM (the split-KV
+                                kernel then only fills the prefill's tail) */
+  int32_t fp8_cache;         /* 1 -> the plan serves mb_attn_forward_fp8: the
+                                pages its prefill requests read get a bf16
+                                staging copy in the workspace (see there) */
 } mb_plan_options_t;
 
 /* Plan summary (mb_plan_info). */
@@ -122,6 +131,10 @@ typedef struct {
   int32_t n_launches;        /* kernels one mb_attn_forward launches          */
   size_t workspace_bytes;
   size_t metadata_bytes;     /* bytes uploaded host->device by the plan       */
+  int32_t prefill_ctas;      /* prefill CTAs mb_attn_forward launches beside the
+                                split-KV kernel (0: no prefill work)         */
+  int32_t staged_pages;      /* fp8 plans: cache pages dequantized to bf16 for
+                                the prefill kernel per forward              */
 } mb_plan_info_t;
 
 typedef struct mb_plan mb_plan_t;
@@ -221,22 +234,31 @@ mb_status_t mb_kv_append_fp8(void* k_codes, void* v_codes, float* k_scale, float
                              cudaStream_t stream);
 
 /* Attention of every planned request over an fp8 cache (layout above):
- * the same result as mb_attn_forward on the dequantized K/V. Only the
- * split-KV path reads fp8 pages: the plan must hold no prefill items (build
- * it with mb_plan_options_t.prefill_min_rows = -1), else
- * MB_ERR_UNSUPPORTED and nothing is enqueued. Q K^T runs on f16 operands
- * (q is rounded once from bf16 to f16, saturating at +-65504; every e4m3
- * code is exact in f16) and P V on bf16 operands, fp32 accumulation. Other
- * arguments, outputs and errors as for mb_attn_forward; all pointers 16-byte
- * aligned (lse 4). */
+ * the same result as mb_attn_forward on the dequantized K/V.
+ *   - Split-KV work (decode rows, small chunks, shared-prefix groups) reads
+ *     the codes directly: Q K^T on the tensor cores in e4m3 (each query row
+ *     written once as two e4m3 rows sq (hi + lo), sq = amax|q| / 448, which
+ *     keeps q to about 2^-8 of each value), the K scales applied to the
+ *     scores, P V on f16 operands (V' = code * v_scale / rho, rho a power of
+ *     two bounding the CTA's V scales), fp32 accumulation.
+ *   - Prefill work needs a plan built with mb_plan_options_t.fp8_cache = 1
+ *     (else MB_ERR_UNSUPPORTED, nothing enqueued). Each forward first
+ *     dequantizes the pages the prefill requests read (decode(code) * scale
+ *     in fp32, rounded once to bf16) into the plan's workspace, once per
+ *     page however many prefill requests map it, then runs the tensor-core
+ *     prefill kernel (bf16 operands, fp32 accumulation) over those pages,
+ *     with the split-KV kernel beside it as in mb_attn_forward.
+ * Other arguments, outputs and errors as for mb_attn_forward; all pointers
+ * 16-byte aligned (lse 4). */
 mb_status_t mb_attn_forward_fp8(const mb_plan_t* plan, const void* q,
                                 const void* k_codes, const void* v_codes,
                                 const float* k_scale, const float* v_scale,
                                 const int32_t* block_table_dev, void* out,
                                 float* lse, cudaStream_t stream);
 
-/* mb_attn_forward_fp8 with per-stage events (MB_STAGE_DECODE; MB_STAGE_COMBINE
- * empty, as in mb_attn_forward_timed). */
+/* mb_attn_forward_fp8 with per-stage events (MB_STAGE_PREFILL covers the
+ * staging dequantization and the prefill kernel; MB_STAGE_DECODE;
+ * MB_STAGE_COMBINE empty, as in mb_attn_forward_timed). */
 mb_status_t mb_attn_forward_fp8_timed(const mb_plan_t* plan, const void* q,
                                       const void* k_codes, const void* v_codes,
                                       const float* k_scale, const float* v_scale,

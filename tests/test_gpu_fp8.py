@@ -256,6 +256,70 @@ def test_fp8_attention_matches_oracle(case):
     check_all(w, out, lse)
 
 
+FP8_PREFILL_CASES = {
+    # (shapes, Hq, Hkv, D, ps, shared_prefix): prefill requests on the
+    # tensor-core kernel over bf16 staging pages, decodes beside them
+    "tiny_mixed_shape": ([(96, 96), (1, 200), (32, 160)], 4, 2, 64, 16, 0),
+    "chunk_and_decodes_d128": ([(300, 1900), (1, 700), (1, 1500), (2, 2300)], 8, 2, 128, 64, 0),
+    "prefills_sharing_pages": ([(64, 320), (48, 304), (40, 296)], 8, 4, 128, 16, 256),
+}
+
+
+@pytest.mark.parametrize("case", sorted(FP8_PREFILL_CASES))
+def test_fp8_prefill_on_tensor_cores_matches_oracle(case):
+    shapes, hq, hkv, d, ps, shared = FP8_PREFILL_CASES[case]
+    w = custom_workload(shapes, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, page_size=ps,
+                        seed=hash(case) % 1000, shared_prefix=shared)
+    out, lse, status, info = run_fp8(w, opts=dict(fp8_cache=1))
+    assert status == 0
+    assert info["n_prefill_items"] > 0 and info["staged_pages"] > 0
+    # every page the prefill requests map is staged once
+    m = w.requests[:, 1] - w.requests[:, 0]
+    pre = np.nonzero(m >= 16)[0]
+    pages = {int(w.block_table[r][b]) for r in pre
+             for b in range(-(-int(w.requests[r, 2]) // ps))}
+    assert info["staged_pages"] == len(pages)
+    check_all(w, out, lse)
+
+
+def test_fp8_chunked_prefill_mix_sampled():
+    # the full chunk (2048 rows at kv 32768) on the tensor-core kernel and
+    # the 64 decodes beside it; sampled heads / rows against the oracle
+    w = W.make_workload("chunked_prefill_mix")
+    out, lse, status, info = run_fp8(w, opts=dict(fp8_cache=1))
+    assert status == 0 and info["n_prefill_items"] > 0 and info["n_decode_items"] > 0
+    s = w.spec
+    g = s.n_q_heads // s.n_kv_heads
+    o = out.to(torch.float64).cpu().numpy()
+    ls = lse.to(torch.float64).cpu().numpy()
+    for r in (0, 1, 40, 64):
+        qs, qe, kv = [int(x) for x in w.requests[r]]
+        k, v = w.logical_kv(r)
+        kd = F.dequantize_rows(*F.quantize_rows(k.float().cpu().numpy()))
+        vd = F.dequantize_rows(*F.quantize_rows(v.float().cpu().numpy()))
+        m = qe - qs
+        rows = [(0, min(m, 64)), (max(0, m - 64), m)] if m > 64 else [(0, m)]
+        for a, b in rows:
+            q = w.q[qs + a:qs + b].to(torch.float64).cpu().numpy()
+            for h in (0, 13, s.n_q_heads - 1):
+                kh = h // g
+                o_ref, l_ref = _attend_rows(q[:, h], kd[:, kh], vd[:, kh], kv - m + a, s.scale)
+                np.testing.assert_allclose(o[qs + a:qs + b, h], o_ref, rtol=TOL, atol=TOL,
+                                           err_msg=f"request {r} head {h} rows {a}:{b}")
+                np.testing.assert_allclose(ls[qs + a:qs + b, h], l_ref, rtol=TOL, atol=TOL)
+
+
+def _attend_rows(q, k, v, first_pos, scale):
+    """fp64 attention of query rows q [n, D] at positions first_pos..first_pos
+    + n - 1 over keys k, v [>= first_pos + n, D] (row i sees keys <= its
+    position), through the oracle's own routine: the rows are the last n new
+    rows of a request whose history is everything before first_pos."""
+    n = q.shape[0]
+    kv = first_pos + n
+    o, l = OA.attend(q[:, None, :], k[:kv, None, :], v[:kv, None, :], scale)
+    return o[:, 0], l[:, 0]
+
+
 def test_fp8_forward_rejects_prefill_plans():
     w = custom_workload([(200, 200), (1, 50)], n_q_heads=4, n_kv_heads=2, head_dim=64,
                         page_size=16)
