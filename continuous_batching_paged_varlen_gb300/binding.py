@@ -59,7 +59,8 @@ class PlanInfo(ctypes.Structure):
                 ("cascade_keys", ctypes.c_int32), ("kv_chunk", ctypes.c_int32),
                 ("total_q", ctypes.c_int32), ("n_launches", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_size_t), ("metadata_bytes", ctypes.c_size_t),
-                ("prefill_ctas", ctypes.c_int32), ("staged_pages", ctypes.c_int32)]
+                ("prefill_ctas", ctypes.c_int32), ("staged_pages", ctypes.c_int32),
+                ("splitkv_copies", ctypes.c_int32)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -381,6 +381,7 @@ mb_status_t mb_attn_forward_timed(const mb_plan_t* plan, const void* q, const vo
     a.status = status;
     a.after_prefill = d.n_prefill_items > 0 ? 1 : 0;
     a.done_counter = reinterpret_cast<int32_t*>(ws + kDoneCounterOffset);
+    a.copies = d.decode_copies;
     a.k_map = &km;
     a.v_map = &vm;
     rec(MB_STAGE_DECODE, 0);

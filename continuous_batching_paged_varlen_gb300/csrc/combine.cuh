@@ -114,20 +114,28 @@ __device__ __forceinline__ void merge_listed_rows(const int4* list, int nl, cons
 // threads: called by all kThreads threads after a __syncthreads that follows
 // every partial write (and its __threadfence) of this CTA; thread r counts
 // row r. scratch: >= 4 * 129 words of shared memory nobody else uses.
+// With `pre`, thread r < n_rows passes its row's merge reference and flat
+// output row (q_index * Hq + q_head), loaded earlier, so that no dependent
+// global load sits on the CTA's exit path; without, they are read here.
 template <int D, int kThreads>
-__device__ __forceinline__ void merge_completed_rows(const MergeArgs& m, uint32_t* scratch) {
+__device__ __forceinline__ void merge_completed_rows(const MergeArgs& m, uint32_t* scratch,
+                                                     bool pre = false, MergeRef my_ref = {},
+                                                     int32_t my_out_row = 0) {
   int* count_n = reinterpret_cast<int*>(scratch + 4 * 128);
   int4* list = reinterpret_cast<int4*>(scratch);
   const int tid = threadIdx.x;
   if (tid == 0) *count_n = 0;
   __syncthreads();
   if (tid < m.n_rows) {
-    const MergeRef ref = m.refs[tid];
+    const MergeRef ref = pre ? my_ref : m.refs[tid];
     if (ref.entry >= 0) {
-      const RowDesc rd = m.rows[tid];
+      int32_t orow = my_out_row;
+      if (!pre) {
+        const RowDesc rd = m.rows[tid];
+        orow = rd.q_index * m.n_q_heads + rd.q_head;
+      }
       if (arrive_partial(m.count + ref.entry, 1, ref.n_slots))
-        list[atomicAdd(count_n, 1)] =
-            make_int4(rd.q_index * m.n_q_heads + rd.q_head, ref.slot_begin, ref.n_slots, 0);
+        list[atomicAdd(count_n, 1)] = make_int4(orow, ref.slot_begin, ref.n_slots, 0);
     }
   }
   __syncthreads();

@@ -66,7 +66,8 @@ enum {
   B_P_FULL = 2 * kSlots + 2,  // + (j & 1)
   B_O_DONE = 2 * kSlots + 4,  // + (j & 1)
   B_VZ_READY = 2 * kSlots + 6,
-  B_COUNT = 2 * kSlots + 7
+  B_EPI_FULL = 2 * kSlots + 7,  // the 4 softmax warps parked their copies (R > 1)
+  B_COUNT = 2 * kSlots + 8
 };
 
 template <int D>
@@ -88,7 +89,269 @@ struct Layout {
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-template <int D>
+// What the softmax warps share with the rest of the CTA.
+struct SoftmaxShared {
+  uint64_t* bars;
+  volatile int* abort_flag;
+  uint32_t tmem;
+  float* redo;  // [4 * 32][D + 4]: the copies' O (the idle K/V ring, epilogue only)
+  float* redm;  // [4 * 32]: the copies' running max, log2 units
+  float* redl;  // [4 * 32]: the copies' running sum
+};
+
+// Softmax role of warp `warp` (0-3) for rows of W keys per copy. Rows: group
+// g = warp % ngrp of 32 rows, copy c = warp / ngrp, with R = 128 / W copies
+// of each row (ngrp = 4 / R groups). The Q tile holds row 32 g + i in TMEM
+// lane 32 (g + ngrp c) + i for every copy c, so each copy's lane receives
+// the row's scores of every key; copy c takes keys [c W, c W + W) of each
+// tile with its own running max, sum and O accumulator (a split of the
+// row's keys), writes its share of P and zeros elsewhere, and the epilogue
+// merges the copies. Spreading a row over the 4 warps spreads its
+// exponentials over the 4 SM sub-partitions: a few rows (a GQA group's g
+// heads of one decode step) leave the MUFU of one sub-partition the limit
+// otherwise, at ~2k cycles per 128-key tile.
+template <int D, int W>
+__device__ __forceinline__ void softmax_role(const DecodeArgs& a, const DecodeItem& it,
+                                             const SoftmaxShared& sh, const RowDesc rd,
+                                             const bool valid, const int n, const int warp,
+                                             const int lane) {
+  constexpr int R = BN / W;     // copies of a row
+  constexpr int NGRP = 4 / R;   // row groups
+  constexpr int RR = D + 4;     // floats per row of the epilogue buffer
+  uint64_t* bars = sh.bars;
+  const int c = warp / NGRP, g = warp % NGRP;
+  const int col0 = c * W;  // this copy's first key of each tile
+  // visible keys of this row inside the item: [k_begin, min(k_end, vis_end))
+  const int vis_hi = min(it.k_end, rd.vis_end);
+  const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+  const uint32_t o_col = sh.tmem + lane_addr + kColO;
+  const float cs = a.scale_log2;
+  float m = -INFINITY, l = 0.f;
+  bool ok = true;
+  for (int j = 0; j < n; ++j) {
+    const uint32_t s_col = sh.tmem + lane_addr + kColS + 128 * (j & 1);
+    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_S_FULL + (j & 1)], (uint32_t)(j >> 1) & 1u,
+                                           sh.abort_flag, a.status));
+    if (!ok) break;
+    tc_fence_after();
+    uint32_t s[W];
+    if constexpr (W == 128) {
+      tmem_ld128(s_col, *reinterpret_cast<uint32_t(*)[128]>(&s[0]));
+      tmem_ld_wait128(*reinterpret_cast<uint32_t(*)[128]>(&s[0]));
+    } else {
+#pragma unroll
+      for (int h = 0; h < W / 32; ++h) {
+        tmem_ld32(s_col + col0 + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * h]));
+        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&s[32 * h]));
+      }
+    }
+    const int lim = vis_hi - (it.k_begin + j * BN) - col0;  // keys e < lim are visible
+    if (lim < W) {
+#pragma unroll
+      for (int e = 0; e < W; ++e)
+        if (e >= lim) s[e] = __float_as_uint(-INFINITY);
+    }
+    constexpr int NM = W < 16 ? W : 16;
+    float mx[NM];
+#pragma unroll
+    for (int k = 0; k < NM; ++k) mx[k] = __uint_as_float(s[k]);
+#pragma unroll
+    for (int e = NM; e < W; e += NM)
+#pragma unroll
+      for (int k = 0; k < NM; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(s[e + k]));
+#pragma unroll
+    for (int w2 = NM / 2; w2 > 0; w2 >>= 1)
+#pragma unroll
+      for (int k = 0; k < w2; ++k) mx[k] = fmaxf(mx[k], mx[k + w2]);
+    const float m_new = fmaxf(m, mx[0]);
+    float alpha = 1.f;
+    bool need = false;
+    if (m == -INFINITY) {
+      m = m_new;  // nothing accumulated yet (O is written with accumulate off or all-zero P)
+    } else if ((m_new - m) * cs > kRescaleThreshold) {
+      need = true;
+      alpha = fast_exp2((m - m_new) * cs);
+      l *= alpha;
+      m = m_new;
+    }
+    const float mc = (m == -INFINITY) ? 0.f : m * cs;
+    float sum[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t pk[W / 2];
+#pragma unroll
+    for (int e = 0; e < W; e += 2) {
+      const float e0 = fast_exp2(fmaf(__uint_as_float(s[e]), cs, -mc));
+      const float e1 = fast_exp2(fmaf(__uint_as_float(s[e + 1]), cs, -mc));
+      sum[(e >> 1) & 3] += e0 + e1;
+      pk[e >> 1] = pack_bf16x2(e0, e1);
+    }
+    l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+    // P(j) goes over S(j) in buffer j & 1, which PV(j - 2) read last: S(j)
+    // was issued after PV(j - 2), so that PV is done. Only a rescale of O
+    // must wait for PV(j - 1), which accumulates into O (the only PV that
+    // can still run: PV(j) needs this P). So the PV's latency stays off
+    // the per-tile chain unless a copy's max grew by more than 2^8.
+    if (__any_sync(0xffffffffu, need)) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + ((j - 1) & 1)],
+                                             (uint32_t)((j - 1) >> 1) & 1u, sh.abort_flag,
+                                             a.status));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(o_col + cc * 32, o);
+        tmem_ld_wait(o);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+        tmem_st32(o_col + cc * 32, o);
+      }
+    }
+    // P: the first 64 columns of the buffer hold the tile's 128 keys as bf16
+    // pairs; this copy's W keys are its W / 2 columns and every other column
+    // of its lanes is zero, so the PV sums only its own keys
+    if constexpr (W == 128) {
+      tmem_st32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+    } else {
+      uint32_t zero[W / 2];
+#pragma unroll
+      for (int e = 0; e < W / 2; ++e) zero[e] = 0u;
+#pragma unroll
+      for (int k = 0; k < R; ++k) {  // c is the same in every lane of the warp
+        const uint32_t* src = k == c ? pk : zero;
+        if constexpr (W == 64) {
+          tmem_st32(s_col + 32 * k, *reinterpret_cast<const uint32_t(*)[32]>(src));
+        } else {
+          tmem_st16(s_col + 16 * k, src);
+        }
+      }
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[B_P_FULL + (j & 1)]);
+  }
+  if (ok && n > 0)
+    ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + ((n - 1) & 1)],
+                                           (uint32_t)((n - 1) >> 1) & 1u, sh.abort_flag,
+                                           a.status));
+  if (!ok || n == 0) return;
+  tc_fence_after();
+  const bool final_row = rd.dst < 0;
+  const int64_t orow = (int64_t)rd.q_index * a.n_q_heads + rd.q_head;
+  if constexpr (R == 1) {
+    const bool any = l > 0.f;
+    const float inv = any ? 1.f / l : 0.f;
+    const float lse2 = any ? m * cs + log2f(l) : -INFINITY;
+    // the TMEM loads are warp-collective: every lane runs them, whatever its
+    // row; only the stores depend on the row
+    uint4* dst_out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * D);
+    float4* dst_part = reinterpret_cast<float4*>(a.part_o + (int64_t)max(rd.dst, 0) * D);
+#pragma unroll
+    for (int cc = 0; cc < D / 32; ++cc) {
+      uint32_t o[32];
+      tmem_ld32(o_col + cc * 32, o);
+      tmem_ld_wait(o);
+      if (valid && final_row) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv);
+          v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
+          v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
+          v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
+          dst_out[cc * 4 + q4] = v;
+        }
+      } else if (valid) {
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          dst_part[cc * 8 + q4] = make_float4(__uint_as_float(o[q4 * 4 + 0]) * inv,
+                                              __uint_as_float(o[q4 * 4 + 1]) * inv,
+                                              __uint_as_float(o[q4 * 4 + 2]) * inv,
+                                              __uint_as_float(o[q4 * 4 + 3]) * inv);
+      }
+    }
+    if (valid && final_row && a.lse) a.lse[orow] = lse2 * kLn2;
+    if (valid && !final_row) {
+      a.part_lse[rd.dst] = lse2;
+      __threadfence();  // the partial is visible before this CTA counts it
+    }
+  } else {
+    // merge the R copies of each row (splits of its keys): every warp parks
+    // its lanes' max, sum and O, then finishes D / R columns of its row group
+    // with weights 2^(m_c - M), M the largest copy max
+    sh.redm[warp * 32 + lane] = m == -INFINITY ? -INFINITY : m * cs;
+    sh.redl[warp * 32 + lane] = l;
+    float* mine = sh.redo + (warp * 32 + lane) * RR;
+#pragma unroll
+    for (int cc = 0; cc < D / 32; ++cc) {
+      uint32_t o[32];
+      tmem_ld32(o_col + cc * 32, o);
+      tmem_ld_wait(o);
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4)
+        *reinterpret_cast<float4*>(mine + cc * 32 + q4 * 4) =
+            make_float4(__uint_as_float(o[q4 * 4 + 0]), __uint_as_float(o[q4 * 4 + 1]),
+                        __uint_as_float(o[q4 * 4 + 2]), __uint_as_float(o[q4 * 4 + 3]));
+    }
+    // every softmax warp runs when R > 1; a bounded wait, so that a warp
+    // that gave up on an earlier wait cannot leave the others here
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[B_EPI_FULL]);
+    if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_EPI_FULL], 0u, sh.abort_flag, a.status)))
+      return;
+    float mcp[R], wc[R];
+    float M = -INFINITY;
+#pragma unroll
+    for (int cc = 0; cc < R; ++cc) {
+      mcp[cc] = sh.redm[(g + NGRP * cc) * 32 + lane];
+      M = fmaxf(M, mcp[cc]);
+    }
+    float lt = 0.f;
+#pragma unroll
+    for (int cc = 0; cc < R; ++cc) {
+      wc[cc] = M == -INFINITY ? 0.f : fast_exp2(mcp[cc] - M);  // 0 for a copy with no key
+      lt += wc[cc] * sh.redl[(g + NGRP * cc) * 32 + lane];
+    }
+    const bool any = lt > 0.f;
+    const float inv = any ? 1.f / lt : 0.f;
+    const float lse2 = any ? M + log2f(lt) : -INFINITY;
+    constexpr int CW = D / R;  // columns this warp finishes
+    const int cbeg = c * CW;
+    if (valid) {
+#pragma unroll 4
+      for (int q4 = 0; q4 < CW / 4; ++q4) {
+        const int col = cbeg + 4 * q4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int cc = 0; cc < R; ++cc) {
+          const float4 v =
+              *reinterpret_cast<const float4*>(sh.redo + ((g + NGRP * cc) * 32 + lane) * RR + col);
+          acc.x = fmaf(wc[cc], v.x, acc.x);
+          acc.y = fmaf(wc[cc], v.y, acc.y);
+          acc.z = fmaf(wc[cc], v.z, acc.z);
+          acc.w = fmaf(wc[cc], v.w, acc.w);
+        }
+        if (final_row) {
+          uint2 w2;
+          w2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+          w2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + orow * D + col) = w2;
+        } else {
+          *reinterpret_cast<float4*>(a.part_o + (int64_t)rd.dst * D + col) =
+              make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        }
+      }
+      if (c == 0) {
+        if (final_row && a.lse) a.lse[orow] = lse2 * kLn2;
+        if (!final_row) a.part_lse[rd.dst] = lse2;
+      }
+      if (!final_row) __threadfence();  // each copy's columns are visible before the count
+    }
+  }
+}
+
+template <int D, bool kCopies>
 __global__ void __launch_bounds__(kThreads, 1)
     splitkv_kernel(const DecodeArgs a, const int ps_shift,
                    const __grid_constant__ CUtensorMap k_map,
@@ -102,10 +365,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
-  // split rows this CTA completed, to merge before it exits: the count in
-  // the misc words, the list over the Q tile (no longer read by then)
-  int* merge_n = reinterpret_cast<int*>(smem + L::misc_off + 8);
-  int4* merge_list = reinterpret_cast<int4*>(sq);
 
   // the kernel behind this one (the next layer's append, say) may launch now
   pdl_launch_dependents();
@@ -115,7 +374,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nr = it.n_rows;
   const int n = ceil_div(it.k_end - it.k_begin, BN);
   const bool tail_zero = it.k_begin + n * BN > it.k_end;
-  const int active_warps = ceil_div(nr, 32);
+  // the kernel built with kCopies spreads each row's keys over 4 copies in
+  // the 4 softmax warps (see softmax_role) when the CTA has at most 32 rows
+  // and a long key range; otherwise one thread per row. The plan picks that
+  // build when most of its keys sit in such CTAs: the copies' code makes the
+  // kernel larger, which costs a short launch more (instruction fetch) than
+  // the copies save it (measured on a shared-prefix step of 5-tile CTAs)
+  const bool copies = kCopies && n >= kCopyMinTiles && nr <= 32;
+  const int ngrp = copies ? 1 : 4;
+  const int active_warps = ngrp < 4 ? 4 : ceil_div(nr, 32);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
@@ -129,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[B_O_DONE + 0], 1);
     mbar_init(&bars[B_O_DONE + 1], 1);
     mbar_init(&bars[B_VZ_READY], 1);
+    mbar_init(&bars[B_EPI_FULL], 4);
     *abort_flag = 0;
-    *merge_n = 0;
     fence_barrier_init();
   }
   // Only the barriers are shared before the producer starts (a short step
@@ -145,6 +412,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t page0 = 0;
   if (warp == 4 && n > 0 && lane < (BN >> ps_shift))
     page0 = __ldg(btrow + min(first_block + lane, last_block));
+  // each softmax lane's row (group warp % ngrp): its descriptor is loaded
+  // now, so that its latency overlaps the set-up and the Q gather
+  const int my_row = (warp % ngrp) * 32 + lane;
+  const bool row_valid = warp < 4 && warp < active_warps && my_row < nr;
+  RowDesc rd;
+  rd.q_index = 0;
+  rd.q_head = 0;
+  rd.vis_end = 0;
+  rd.dst = -1;
+  if (row_valid) rd = a.rows[it.row_begin + my_row];
+  // thread t < n_rows counts row t's arrival at the end (split rows): its
+  // merge reference and output row, loaded now as well
+  MergeRef my_ref = {-1, 0, 0, 0};
+  int32_t my_out_row = 0;
+  if (a.combine_count && (int)threadIdx.x < nr) {
+    my_ref = a.row_merge[it.row_begin + threadIdx.x];
+    const RowDesc md = a.rows[it.row_begin + threadIdx.x];
+    my_out_row = md.q_index * a.n_q_heads + md.q_head;
+  }
   __syncthreads();
   uint32_t tmem = 0;
   if (warp != 4) {
@@ -165,12 +451,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint4 qv[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
+      // tile row t holds item row 32 ((t / 32) % ngrp) + t % 32: each row
+      // once per copy
       const int idx = gt + k * kGather;
-      const int r = idx / CH, c = idx - r * CH;
+      const int t = idx / CH, c = idx - t * CH;
+      const int r = ((t >> 5) % ngrp) * 32 + (t & 31);
       qv[k] = make_uint4(0u, 0u, 0u, 0u);
       if (idx < BM * CH && r < nr) {
-        const RowDesc rd = a.rows[it.row_begin + r];
-        qv[k] = __ldg(q + ((int64_t)rd.q_index * a.n_q_heads + rd.q_head) * CH + c);
+        const RowDesc qd = a.rows[it.row_begin + r];
+        qv[k] = __ldg(q + ((int64_t)qd.q_index * a.n_q_heads + qd.q_head) * CH + c);
       }
     }
     named_barrier_arrive(2, kThreads);  // the producer's wait below
@@ -324,149 +613,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < active_warps) {
     // ------------------------------------------------------------ softmax
-    const int r = warp * 32 + lane;
-    const bool valid = r < nr;
-    RowDesc rd;
-    rd.q_index = 0;
-    rd.q_head = 0;
-    rd.vis_end = 0;
-    rd.dst = -1;
-    if (valid) rd = a.rows[it.row_begin + r];
-    MergeRef ref = {-1, 0, 0, 0};
-    if (valid && rd.dst >= 0) ref = a.row_merge[it.row_begin + r];
-    // visible keys of this row inside the item: [k_begin, min(k_end, vis_end))
-    const int vis_hi = min(it.k_end, rd.vis_end);
-    const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-    const uint32_t o_col = tmem + lane_addr + kColO;
-    const float c = a.scale_log2;
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const uint32_t s_col = tmem + lane_addr + kColS + 128 * (j & 1);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_S_FULL + (j & 1)], (uint32_t)(j >> 1) & 1u,
-                                             abort_flag, a.status));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t s[128];
-      tmem_ld128(s_col, s);
-      tmem_ld_wait128(s);
-      const int lim = vis_hi - (it.k_begin + j * BN);  // keys e < lim are visible
-      if (lim < BN) {
-#pragma unroll
-        for (int e = 0; e < 128; ++e)
-          if (e >= lim) s[e] = __float_as_uint(-INFINITY);
-      }
-      float mx[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) mx[k] = __uint_as_float(s[k]);
-#pragma unroll
-      for (int e = 16; e < 128; e += 16)
-#pragma unroll
-        for (int k = 0; k < 16; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(s[e + k]));
-#pragma unroll
-      for (int w2 = 8; w2 > 0; w2 >>= 1)
-#pragma unroll
-        for (int k = 0; k < w2; ++k) mx[k] = fmaxf(mx[k], mx[k + w2]);
-      const float m_new = fmaxf(m, mx[0]);
-      float alpha = 1.f;
-      bool need = false;
-      if (m == -INFINITY) {
-        m = m_new;  // nothing accumulated yet (O is written with accumulate off or all-zero P)
-      } else if ((m_new - m) * c > kRescaleThreshold) {
-        need = true;
-        alpha = fast_exp2((m - m_new) * c);
-        l *= alpha;
-        m = m_new;
-      }
-      const float mc = (m == -INFINITY) ? 0.f : m * c;
-      float sum[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[64];
-#pragma unroll
-      for (int e = 0; e < 128; e += 2) {
-        const float e0 = fast_exp2(fmaf(__uint_as_float(s[e]), c, -mc));
-        const float e1 = fast_exp2(fmaf(__uint_as_float(s[e + 1]), c, -mc));
-        sum[(e >> 1) & 3] += e0 + e1;
-        pk[e >> 1] = pack_bf16x2(e0, e1);
-      }
-      l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
-      // P(j) goes over S(j) in buffer j & 1, which PV(j - 2) read last: S(j)
-      // was issued after PV(j - 2), so that PV is done. Only a rescale of O
-      // must wait for PV(j - 1), which accumulates into O (the only PV that
-      // can still run: PV(j) needs this P). So the PV's latency stays off
-      // the per-tile chain unless a row's max grew by more than 2^8.
-      if (__any_sync(0xffffffffu, need)) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + ((j - 1) & 1)],
-                                               (uint32_t)((j - 1) >> 1) & 1u,
-                                               abort_flag, a.status));
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(o_col + cc * 32, o);
-          tmem_ld_wait(o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(o_col + cc * 32, o);
-        }
-      }
-      tmem_st32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_P_FULL + (j & 1)]);
-    }
-    if (ok && n > 0)
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_O_DONE + ((n - 1) & 1)],
-                                             (uint32_t)((n - 1) >> 1) & 1u,
-                                             abort_flag, a.status));
-    if (ok && n > 0) {
-      tc_fence_after();
-      const bool any = l > 0.f;
-      const float inv = any ? 1.f / l : 0.f;
-      const float lse2 = any ? m * c + log2f(l) : -INFINITY;
-      // the TMEM loads are warp-collective: every lane runs them, whatever
-      // its row; only the stores depend on the row
-      const bool final_row = rd.dst < 0;
-      const int64_t orow = (int64_t)rd.q_index * a.n_q_heads + rd.q_head;
-      uint4* dst_out =
-          reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * D);
-      float4* dst_part = reinterpret_cast<float4*>(a.part_o + (int64_t)max(rd.dst, 0) * D);
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(o_col + cc * 32, o);
-        tmem_ld_wait(o);
-        if (valid && final_row) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
-            dst_out[cc * 4 + q4] = v;
-          }
-        } else if (valid) {
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            dst_part[cc * 8 + q4] = make_float4(__uint_as_float(o[q4 * 4 + 0]) * inv,
-                                                __uint_as_float(o[q4 * 4 + 1]) * inv,
-                                                __uint_as_float(o[q4 * 4 + 2]) * inv,
-                                                __uint_as_float(o[q4 * 4 + 3]) * inv);
-        }
-      }
-      if (valid && final_row && a.lse) a.lse[orow] = lse2 * kLn2;
-      if (valid && !final_row) a.part_lse[rd.dst] = lse2;
-    }
-    // one arrival per partial row, also after an abort (the counters must
-    // stay in step for the next launch); the partial is fenced before it
-    if (valid && rd.dst >= 0) {
-      __threadfence();
-      if (dev::arrive_partial(a.combine_count + ref.entry, 1, ref.n_slots))
-        merge_list[atomicAdd(merge_n, 1)] =
-            make_int4(rd.q_index * a.n_q_heads + rd.q_head, ref.slot_begin, ref.n_slots, 0);
+    SoftmaxShared sh;
+    sh.bars = bars;
+    sh.abort_flag = abort_flag;
+    sh.tmem = tmem;
+    // the epilogue's buffers: the K/V ring, idle once the last PV is done
+    sh.redo = reinterpret_cast<float*>(skv);
+    sh.redm = sh.redo + 128 * (D + 4);
+    sh.redl = sh.redm + 128;
+    if constexpr (kCopies) {
+      if (copies)
+        softmax_role<D, 32>(a, it, sh, rd, row_valid, n, warp, lane);
+      else
+        softmax_role<D, 128>(a, it, sh, rd, row_valid, n, warp, lane);
+    } else {
+      softmax_role<D, 128>(a, it, sh, rd, row_valid, n, warp, lane);
     }
   }
 
@@ -476,13 +637,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  const int nl = *reinterpret_cast<volatile int*>(merge_n);
-  if (nl > 0) {
-    // the other CTAs fenced their partials before arriving: order this
-    // CTA's reads after the arrivals it observed
-    __threadfence();
-    dev::merge_listed_rows<D, kThreads>(merge_list, nl, a.part_o, a.part_lse,
-                                        static_cast<__nv_bfloat16*>(a.out), a.lse);
+  if (a.combine_count) {
+    // one arrival per split row (also after an abort: the counters must stay
+    // in step for the next launch); the CTA whose arrival completes a row
+    // merges it. Every partial write of this CTA was fenced before the
+    // barrier above. Scratch: the Q tile, no longer read.
+    dev::MergeArgs mg;
+    mg.rows = a.rows + it.row_begin;
+    mg.refs = a.row_merge + it.row_begin;
+    mg.n_rows = nr;
+    mg.count = a.combine_count;
+    mg.part_o = a.part_o;
+    mg.part_lse = a.part_lse;
+    mg.n_q_heads = a.n_q_heads;
+    mg.out = static_cast<__nv_bfloat16*>(a.out);
+    mg.lse = a.lse;
+    dev::merge_completed_rows<D, kThreads>(mg, reinterpret_cast<uint32_t*>(sq), true, my_ref,
+                                           my_out_row);
   }
   if (!dep_wait && threadIdx.x == 0) {
     // started under the prefill kernel's tail: the grid must not complete
@@ -496,38 +667,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-}  // namespace
-
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, bool overlap_previous) {
-  if (a.n_items <= 0) return cudaSuccess;
-  const int ps_shift = __builtin_ctz((unsigned)a.page_size);
+template <int D, bool kCopies>
+cudaError_t launch_d(const DecodeArgs& a, cudaStream_t s, bool overlap_previous, int ps_shift) {
+  static OncePerDevice setup;
+  cudaError_t e = setup.run([](int) {
+    return cudaFuncSetAttribute(splitkv_kernel<D, kCopies>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Layout<D>::kAlloc);
+  });
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.n_items);
   cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Layout<D>::kAlloc;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap_previous ? 1 : 0;
-  static OncePerDevice setup128, setup64;
-  cudaError_t e;
-  if (a.head_dim == 128) {
-    cfg.dynamicSmemBytes = Layout<128>::kAlloc;
-    e = setup128.run([](int) {
-      return cudaFuncSetAttribute(splitkv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)Layout<128>::kAlloc);
-    });
-    if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, splitkv_kernel<128>, a, ps_shift, *a.k_map, *a.v_map);
-  }
-  cfg.dynamicSmemBytes = Layout<64>::kAlloc;
-  e = setup64.run([](int) {
-    return cudaFuncSetAttribute(splitkv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)Layout<64>::kAlloc);
-  });
-  if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, splitkv_kernel<64>, a, ps_shift, *a.k_map, *a.v_map);
+  return cudaLaunchKernelEx(&cfg, splitkv_kernel<D, kCopies>, a, ps_shift, *a.k_map, *a.v_map);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, bool overlap_previous) {
+  if (a.n_items <= 0) return cudaSuccess;
+  const int ps_shift = __builtin_ctz((unsigned)a.page_size);
+  if (a.head_dim == 128)
+    return a.copies ? launch_d<128, true>(a, s, overlap_previous, ps_shift)
+                    : launch_d<128, false>(a, s, overlap_previous, ps_shift);
+  return a.copies ? launch_d<64, true>(a, s, overlap_previous, ps_shift)
+                  : launch_d<64, false>(a, s, overlap_previous, ps_shift);
 }
 
 }  // namespace mb

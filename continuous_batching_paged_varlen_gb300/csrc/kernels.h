@@ -86,6 +86,9 @@ struct DecodeArgs {
   // every global write wait for it; history keys stream at once.
   int32_t after_prefill;
   int32_t* done_counter;
+  // 1: the build that spreads a row's keys over copies in the softmax warps
+  // (CTAs of <= 32 rows with long key ranges); 0: one thread per row
+  int32_t copies;
   const CUtensorMap* k_map;  // host copies, passed by value to the kernel
   const CUtensorMap* v_map;
 };

@@ -37,6 +37,8 @@ constexpr int kRowsPerDecodeItem = 128; // query rows one split-KV CTA owns (TME
 constexpr int kPrefillTileM = 128;      // query rows per prefill tile (one TMEM accumulator)
 constexpr int kPrefillTileN = 128;      // keys per prefill KV tile
 constexpr int kPrefillCtaRows = 256;    // query rows per prefill CTA (two tiles)
+constexpr int kCopyMinTiles = 16;       // 128-key tiles from which a split-KV CTA of <= 32
+                                        // rows spreads each row's keys over 4 copies
 
 // One CTA of the split-KV kernel: query rows (all of one KV head) against
 // the key range [k_begin, k_end) of one block-table row.
@@ -99,6 +101,7 @@ struct PlanDevice {
   int32_t n_q_heads, n_kv_heads, head_dim, page_size, num_pages, max_blocks;
   int32_t total_q;
   int32_t prefill_ctas;  // prefill grid when the split-KV kernel runs beside it
+  int32_t decode_copies;  // split-KV build with row copies (most keys in long CTAs of <= 32 rows)
   float scale;
   size_t off_decode_items, off_rows, off_prefill_items, off_combine, off_row_merge,
       off_combine_count, off_part_lse, off_part_o;

@@ -187,6 +187,7 @@ extern "C" mb_status_t mb_attn_forward_noalloc(const mb_plan_t* plan, const void
     a.status = status;
     a.after_prefill = 0;
     a.done_counter = reinterpret_cast<int32_t*>(ws + kDoneCounterOffset);
+    a.copies = d.decode_copies;
     a.k_map = &km;
     a.v_map = &vm;
     if (launch_decode(a, stream) != cudaSuccess) return MB_ERR_CUDA;

@@ -503,6 +503,19 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
     pitems.swap(sorted);
   }
 
+  // ---- split-KV build: row copies when most keys sit in long CTAs of
+  // <= 32 rows (see splitkv_kernel) ---------------------------------------
+  int32_t decode_copies = 0;
+  {
+    int64_t long_tiles = 0, all_tiles = 0;
+    for (const DecodeItem& it : items) {
+      const int64_t t = (it.k_end - it.k_begin + 127) / 128;
+      all_tiles += t;
+      if (t >= kCopyMinTiles && it.n_rows <= 32) long_tiles += t;
+    }
+    decode_copies = 2 * long_tiles >= all_tiles && all_tiles > 0 ? 1 : 0;
+  }
+
   // ---- SMs of the prefill grid beside the split-KV kernel ---------------
   int32_t prefill_ctas = std::min<int32_t>((int32_t)pitems.size(), kSms);
   if (!pitems.empty() && !items.empty()) {
@@ -557,6 +570,7 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
   d.max_blocks = mb;
   d.total_q = total_q;
   d.prefill_ctas = pitems.empty() ? 0 : prefill_ctas;
+  d.decode_copies = decode_copies;
   d.scale = cfg->scale > 0.f ? cfg->scale : 1.0f / sqrtf((float)D);
   size_t off = kStatusBytes;
   d.off_decode_items = off;
@@ -635,6 +649,7 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
   info.metadata_bytes = d.metadata_bytes;
   info.prefill_ctas = d.prefill_ctas;
   info.staged_pages = d.n_stage_pages;
+  info.splitkv_copies = d.decode_copies;
   return MB_OK;
 }
 

@@ -135,6 +135,9 @@ typedef struct {
                                 split-KV kernel (0: no prefill work)         */
   int32_t staged_pages;      /* fp8 plans: cache pages dequantized to bf16 for
                                 the prefill kernel per forward              */
+  int32_t splitkv_copies;    /* 1: the split-KV build that spreads each row's
+                                keys over copies in the softmax warps (most
+                                keys in CTAs of <= 32 rows and >= 16 tiles) */
 } mb_plan_info_t;
 
 typedef struct mb_plan mb_plan_t;

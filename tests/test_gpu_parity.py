@@ -199,6 +199,48 @@ def test_edge_cases(case, opt):
             assert_request_close(w, out, lse, r)
 
 
+# Long key ranges (>= 16 tiles of 128 keys per split-KV CTA). A plan with
+# most of its keys in such CTAs of <= 32 rows runs the split-KV build that
+# spreads each row's keys over 4 copies in the softmax warps; its CTAs with
+# more rows or short ranges keep one thread per row. Cases: copies alone,
+# with partials, a shared-prefix group, and mixed with a 40-row CTA; plans
+# that stay on the other build.
+COPY_CASES = {
+    # (shapes, workload kw, planner options, split-KV build expected)
+    "4_rows_copies": ([(1, 5000), (1, 2600)], dict(n_q_heads=8, n_kv_heads=2, head_dim=128,
+                                                   page_size=64), dict(kv_chunk=8192), 1),
+    "split_rows_copies": ([(1, 9000), (2, 7000)], dict(n_q_heads=8, n_kv_heads=2,
+                                                       head_dim=128, page_size=64),
+                          dict(kv_chunk=2560), 1),
+    "cascade_32_rows_copies": ([(1, 4200 + 13 * i) for i in range(8)],
+                               dict(n_q_heads=8, n_kv_heads=2, head_dim=128, page_size=64,
+                                    shared_prefix=4096), dict(kv_chunk=4096), 1),
+    "copies_with_a_40_row_cta": ([(1, 6000), (10, 5000), (1, 7000)],
+                                 dict(n_q_heads=8, n_kv_heads=2, head_dim=64, page_size=32),
+                                 dict(kv_chunk=8192, prefill_min_rows=-1), 1),
+    "48_rows_one_per_thread": ([(12, 4000)], dict(n_q_heads=8, n_kv_heads=2, head_dim=128,
+                                                  page_size=64),
+                               dict(kv_chunk=8192, prefill_min_rows=-1), 0),
+    "100_rows_one_per_thread": ([(25, 3000)], dict(n_q_heads=8, n_kv_heads=2, head_dim=64,
+                                                   page_size=32),
+                                dict(kv_chunk=8192, prefill_min_rows=-1), 0),
+}
+
+
+@pytest.mark.parametrize("case", sorted(COPY_CASES))
+def test_long_ranges_split_kv_builds(case):
+    shapes, kw, opts, build = COPY_CASES[case]
+    w = custom_workload(shapes, seed=sum(map(ord, case)), **kw)
+    kc, vc, cfg = fill_cache(w)
+    out, lse, status, info = run_forward(w, kc, vc, cfg, B.options(**opts))
+    assert status == 0
+    assert info["splitkv_copies"] == build
+    if "cascade" in case:
+        assert info["n_cascade_groups"] == 1
+    for r in range(w.n_requests):
+        assert_request_close(w, out, lse, r)
+
+
 def test_deterministic_and_empty():
     w = W.make_workload("tiny_mixed")
     kc, vc, cfg = fill_cache(w)
