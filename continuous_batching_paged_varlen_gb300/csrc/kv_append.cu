@@ -15,8 +15,6 @@
 // copy is bit-exact.
 #include <cuda_runtime.h>
 
-#include <type_traits>
-
 #include "../../include/mb.h"
 #include "kernels.h"
 #include "mb_device.cuh"
@@ -116,120 +114,62 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new,
 // row, scale = amax(|row|) / 448, code = e4m3(x / scale) rounded to nearest
 // (ties to even), saturating; a zero row gets scale 0 and zero codes. The
 // quotient is one IEEE fp32 division, so the codes are reproducible.
-// A warp quantizes (token, KV head, K or V) rows, kFp8Rows at a time: their
-// loads are all issued before the first is used (a row is only D values,
-// so one at a time would leave the warp waiting on memory). Each lane holds
-// D/32 consecutive values of a row. Warps stride over all rows.
+// One warp per row: each lane holds D/32 consecutive values.
 namespace mb {
 namespace {
 
-constexpr int kFp8Warps = 8;  // per block
-constexpr int kFp8Rows = 4;   // rows in flight per warp
-
 template <int D>
-__global__ void __launch_bounds__(32 * kFp8Warps) kv_append_fp8_kernel(
+__global__ void __launch_bounds__(128) kv_append_fp8_kernel(
     uint8_t* __restrict__ k8, uint8_t* __restrict__ v8, float* __restrict__ ks,
     float* __restrict__ vs, const __nv_bfloat16* __restrict__ kn,
-    const __nv_bfloat16* __restrict__ vn, const int32_t* __restrict__ slots, int32_t T,
-    int32_t Hkv, int32_t ps_shift, int64_t n_slots, int32_t* status) {
+    const __nv_bfloat16* __restrict__ vn, const int32_t* __restrict__ slots, int32_t Hkv,
+    int32_t ps_shift, int64_t n_slots, int32_t* status) {
   constexpr int E = D / 32;  // values per lane (4 for D = 128, 2 for D = 64)
-  using Vec = typename std::conditional<E == 4, uint2, uint32_t>::type;
   dev::pdl_launch_dependents();
   dev::pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const uint32_t row_len = 2u * (uint32_t)Hkv;      // rows per token
-  const uint32_t n_rows = (uint32_t)T * row_len;     // < 2^31 (checked by the launcher)
-  const uint32_t n_warps = gridDim.x * kFp8Warps;
-  for (uint32_t r0 = blockIdx.x * kFp8Warps + (threadIdx.x >> 5); r0 < n_rows;
-       r0 += n_warps * kFp8Rows) {
-    // every load first (the row's values do not depend on its slot), then
-    // the checks and the arithmetic
-    Vec raw[kFp8Rows];
-    int32_t slot[kFp8Rows];
-    uint32_t t[kFp8Rows], row[kFp8Rows];
+  const int t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int32_t slot = __ldg(slots + t);
+  if (slot < 0) return;
+  if ((int64_t)slot >= n_slots) {
+    if (threadIdx.x == 0) dev::set_status(status, MB_ERR_DEVICE_INDEX);
+    return;
+  }
+  const int32_t page = slot >> ps_shift;
+  const int32_t off = slot & ((1 << ps_shift) - 1);
+  for (int row = warp; row < 2 * Hkv; row += 4) {
+    const int h = row < Hkv ? row : row - Hkv;
+    const __nv_bfloat16* src = (row < Hkv ? kn : vn) + ((int64_t)t * Hkv + h) * D + E * lane;
+    float x[E];
+    float amax = 0.f;
 #pragma unroll
-    for (int q = 0; q < kFp8Rows; ++q) {
-      const uint32_t grow = r0 + q * n_warps;
-      slot[q] = -1;
-      if (grow >= n_rows) continue;
-      t[q] = grow / row_len;
-      row[q] = grow - t[q] * row_len;
-      const bool v = row[q] >= (uint32_t)Hkv;
-      const uint32_t h = v ? row[q] - Hkv : row[q];
-      slot[q] = __ldg(slots + t[q]);
-      raw[q] = __ldg(reinterpret_cast<const Vec*>((v ? vn : kn) +
-                                                  ((size_t)t[q] * Hkv + h) * D) + lane);
-    }
-    int64_t drow[kFp8Rows];
-    bool is_v[kFp8Rows];
-#pragma unroll
-    for (int q = 0; q < kFp8Rows; ++q) {
-      drow[q] = -1;
-      is_v[q] = false;
-      if (slot[q] < 0) continue;  // past the rows, or a padding row
-      if ((int64_t)slot[q] >= n_slots) {
-        if (row[q] == 0 && lane == 0) dev::set_status(status, MB_ERR_DEVICE_INDEX);
-        continue;
-      }
-      is_v[q] = row[q] >= (uint32_t)Hkv;
-      const int h = (int)(is_v[q] ? row[q] - Hkv : row[q]);
-      drow[q] = (((int64_t)(slot[q] >> ps_shift) * Hkv + h) << ps_shift) +
-                (slot[q] & ((1 << ps_shift) - 1));
+    for (int e = 0; e < E; ++e) {
+      x[e] = __bfloat162float(src[e]);
+      amax = fmaxf(amax, fabsf(x[e]));
     }
 #pragma unroll
-    for (int q = 0; q < kFp8Rows; ++q) {
-      if (drow[q] < 0) continue;  // warp-uniform: every lane has the same row
-      uint32_t w[E / 2];
-      if constexpr (E == 4) {
-        w[0] = raw[q].x;
-        w[1] = raw[q].y;
-      } else {
-        w[0] = raw[q];
-      }
-      float x[E];
-      float amax = 0.f;
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = __fdiv_rn(amax, 448.0f);
+    uint8_t code[E];
 #pragma unroll
-      for (int e = 0; e < E / 2; ++e) {
-        x[2 * e] = dev::bf16_lo(w[e]);
-        x[2 * e + 1] = dev::bf16_hi(w[e]);
-        amax = dev::fmax3(amax, fabsf(x[2 * e]), fabsf(x[2 * e + 1]));
+    for (int e = 0; e < E; e += 2) {
+      uint16_t pair = 0;
+      if (scale > 0.f) {
+        const float a = __fdiv_rn(x[e], scale), b = __fdiv_rn(x[e + 1], scale);
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(b), "f"(a));
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const float scale = __fdiv_rn(amax, 448.0f);
-      // code = e4m3(x / scale) with the quotient an IEEE fp32 division, as
-      // the format's definition here fixes it. y = x * rcp(scale) (the
-      // reciprocal correctly rounded) is within 3 fp32 units of that
-      // quotient: it rounds to the same e4m3 code unless it lies within a
-      // few units of an e4m3 rounding midpoint (the fp32 fraction below the
-      // code's 3 mantissa bits equal to one half) or outside the normal e4m3
-      // range [2^-6, 2^9); those rare values take the division itself.
-      const float r = __frcp_rn(scale);
-      auto quotient = [&](float xv) -> float {
-        const float y = xv * r;
-        const float ay = fabsf(y);
-        const int off_mid = (int)(__float_as_uint(y) & 0xFFFFFu) - 0x80000;
-        if (!(ay >= 0x1p-6f && ay < 0x1p9f) || (off_mid >= -4 && off_mid <= 4))
-          return __fdiv_rn(xv, scale);
-        return y;
-      };
-      uint32_t packed = 0;
-#pragma unroll
-      for (int e = 0; e < E; e += 2) {
-        uint16_t pair = 0;
-        if (scale > 0.f) {
-          const float a = quotient(x[e]), b = quotient(x[e + 1]);
-          asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(b), "f"(a));
-        }
-        packed |= (uint32_t)pair << (8 * e);
-      }
-      uint8_t* dst = (is_v[q] ? v8 : k8) + drow[q] * D + E * lane;
-      if constexpr (E == 4)
-        *reinterpret_cast<uint32_t*>(dst) = packed;
-      else
-        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
-      if (lane == 0) (is_v[q] ? vs : ks)[drow[q]] = scale;
+      code[e] = (uint8_t)(pair & 0xff);
+      code[e + 1] = (uint8_t)(pair >> 8);
     }
+    const int64_t drow = (((int64_t)page * Hkv + h) << ps_shift) + off;
+    uint8_t* dst = (row < Hkv ? k8 : v8) + drow * D + E * lane;
+    if constexpr (E == 4) {
+      *reinterpret_cast<uint32_t*>(dst) = (uint32_t)code[0] | ((uint32_t)code[1] << 8) |
+                                          ((uint32_t)code[2] << 16) | ((uint32_t)code[3] << 24);
+    } else {
+      *reinterpret_cast<uint16_t*>(dst) = (uint16_t)(code[0] | (code[1] << 8));
+    }
+    if (lane == 0) (row < Hkv ? ks : vs)[drow] = scale;
   }
 }
 
@@ -303,18 +243,10 @@ cudaError_t launch_kv_append_fp8(void* k8, void* v8, float* ks, float* vs, const
                                  int32_t num_pages, int32_t* status, cudaStream_t s) {
   const int ps_shift = __builtin_ctz((unsigned)page_size);
   const int64_t n_slots = (int64_t)num_pages * page_size;
-  // enough warps for every row in one pass, at most 16 blocks per SM; row
-  // indices are 32-bit in the kernel
-  const int64_t rows = (int64_t)T * 2 * n_kv_heads;
-  if (rows >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
-  const int64_t per_block = (int64_t)kFp8Warps * kFp8Rows;
-  const int64_t want = (rows + per_block - 1) / per_block;
-  const unsigned grid = (unsigned)(want < 152 * 16 ? want : 152 * 16);
   return launch_programmatic(
-      head_dim == 128 ? kv_append_fp8_kernel<128> : kv_append_fp8_kernel<64>, dim3(grid),
-      dim3(32 * kFp8Warps), 0, s, (uint8_t*)k8, (uint8_t*)v8, ks, vs,
-      (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, slots, T, n_kv_heads, ps_shift,
-      n_slots, status);
+      head_dim == 128 ? kv_append_fp8_kernel<128> : kv_append_fp8_kernel<64>, dim3((unsigned)T),
+      dim3(128), 0, s, (uint8_t*)k8, (uint8_t*)v8, ks, vs, (const __nv_bfloat16*)k_new,
+      (const __nv_bfloat16*)v_new, slots, n_kv_heads, ps_shift, n_slots, status);
 }
 
 }  // namespace mb
