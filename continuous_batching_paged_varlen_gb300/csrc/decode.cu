@@ -25,10 +25,23 @@
 //               gathered rows, N 128 keys, K = D) into a double-buffered TMEM
 //               tile and O += P V (P from TMEM, V from shared memory). The
 //               tensor core is mostly idle: it only spares the CUDA cores.
-//   warps 0-3   one thread per query row; only warps that own real rows run:
-//               TMEM load of the row's 128 scores, mask, online max / sum in
-//               the log2 domain, P back into TMEM over the scores, rare O
-//               rescale, epilogue.
+//   warps 0-3   softmax: TMEM load of a row's scores, mask, online max / sum
+//               in the log2 domain, P back into TMEM over the scores, rare O
+//               rescale, epilogue. One thread per query row (only warps that
+//               own real rows run), or, in the kCopies build for CTAs of at
+//               most 32 rows and at least kCopyMinTiles key tiles (a decode
+//               step's GQA group), each row copied into one lane of each of
+//               the 4 warps, each copy keeping its own online softmax over 32
+//               of every tile's 128 keys; the copies merge in the epilogue.
+//               One row's exponentials then run on all 4 SM sub-partitions
+//               instead of one, which is what paced the 4-row CTAs.
+// Launch overlap: the kernel lets the next launch on the stream start at
+// once and waits (griddepcontrol) for the launch before it only where it
+// must: behind the KV append, before it reads q or a tile that holds this
+// step's rows, reuses a ring slot or writes anything, so that history tiles
+// stream while the append runs; behind its own forward's prefill kernel it
+// runs on the SMs the prefill grid leaves free and its last CTA waits for the
+// prefill before the grid completes.
 // Every wait is bounded; on a timeout the CTA raises its abort flag, drains
 // what it issued, frees its TMEM and returns.
 #include <cuda_runtime.h>

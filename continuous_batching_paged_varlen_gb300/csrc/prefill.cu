@@ -12,7 +12,10 @@
 // The grid is persistent: one CTA per SM (each holds its SM's 512 TMEM
 // columns) walks a share of the planner's heavy-first item list, so the next
 // item's Q and first K/V tiles load, and its first S MMAs run, while the
-// current item's last tiles and epilogue finish.
+// current item's last tiles and epilogue finish. When the iteration also has
+// split-KV work, the plan may cap the grid below the SM count: the split-KV
+// kernel, launched behind this one, starts at once on the SMs left free and
+// takes each SM whose CTA has finished its share.
 //
 // Roles (384 threads, three warpgroups):
 //   warps 0-3   softmax of query tile A, warps 4-7 softmax of tile B: one

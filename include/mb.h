@@ -206,7 +206,10 @@ mb_status_t mb_check_append_targets(const mb_request_t* reqs, int32_t n_reqs,
  * with another request (the caller's contract; mb_check_append_targets
  * checks it on the host). A slot >= num_pages*ps is
  * skipped and sets bit (1 << MB_ERR_DEVICE_INDEX) in *status_dev
- * (nullable device int32). T = 0 enqueues nothing. Asynchronous on stream. */
+ * (nullable device int32). T = 0 enqueues nothing. Asynchronous on stream:
+ * the kernel may start under the tail of the launch before it on `stream`
+ * (programmatic dependent launch) and waits for that launch to complete
+ * before it reads or writes any memory. */
 mb_status_t mb_kv_append(void* k_cache, void* v_cache, const void* k_new,
                          const void* v_new, const int32_t* slot_mapping,
                          int32_t T, const mb_config_t* cfg, int32_t* status_dev,
@@ -228,8 +231,8 @@ mb_status_t mb_kv_append(void* k_cache, void* v_cache, const void* k_new,
  * largest e4m3 value) and code_i = e4m3(x_i / scale) (one IEEE fp32
  * division, round to nearest even, saturating at +-448, the sign kept for
  * values that round to zero); an all-zero row gets scale 0 and codes 0.
- * Slot rules, status bits, alignment (every pointer 16-byte aligned) and
- * errors as for mb_kv_append. */
+ * Slot rules, status bits, alignment (every pointer 16-byte aligned),
+ * launch order and errors as for mb_kv_append. */
 mb_status_t mb_kv_append_fp8(void* k_codes, void* v_codes, float* k_scale, float* v_scale,
                              const void* k_new, const void* v_new,
                              const int32_t* slot_mapping, int32_t T,
@@ -297,7 +300,7 @@ mb_status_t mb_rope_table(float* cos_sin, int32_t max_position, int32_t head_dim
  * cache write; both set bit (1 << MB_ERR_DEVICE_INDEX) in *status_dev
  * (nullable device int32). Pages written must not be shared with another
  * request (the caller's contract). T = 0 enqueues nothing. Asynchronous on
- * stream; host errors as for mb_kv_append. */
+ * stream, launch order and host errors as for mb_kv_append. */
 mb_status_t mb_rope_kv_append(void* q, void* k_cache, void* v_cache, const void* k_new,
                               const void* v_new, const int32_t* positions,
                               const int32_t* slot_mapping, int32_t T, const float* cos_sin,
@@ -343,11 +346,17 @@ mb_status_t mb_attn_plan_ex(const mb_request_t* reqs, int32_t n_reqs,
  * request covers are not written), lse [total_q, Hq] fp32 natural-log
  * log-sum-exp of the scaled visible scores (nullable). No device->host
  * traffic and no allocation: the launch sequence can be captured in a CUDA
- * graph. When the plan holds both prefill and split-KV work, the prefill
- * kernel is launched first and the split-KV kernel overlaps its end
- * (programmatic dependent launch on the same stream); everything is ordered
- * on `stream` as usual. Device-detected errors go to the workspace status
- * word. */
+ * graph. Launch order (programmatic dependent launch on the same stream):
+ * the split-KV kernel starts under the tail of the launch before it (the
+ * KV append, say) and streams history key tiles at once, but waits for that
+ * launch to complete before it reads q or a key tile holding this step's
+ * rows and before it writes anything. When the plan holds both kinds of
+ * work, the prefill kernel is launched first on info.prefill_ctas SMs (it
+ * starts once the launch before it has completed) and the split-KV kernel
+ * runs beside it on the other SMs, then on each SM a prefill CTA leaves;
+ * its last CTA waits for the prefill kernel. Whatever is enqueued on
+ * `stream` after the call sees out and lse. Device-detected errors go to
+ * the workspace status word. */
 mb_status_t mb_attn_forward(const mb_plan_t* plan, const void* q,
                             const void* k_cache, const void* v_cache,
                             const int32_t* block_table_dev, void* out,
