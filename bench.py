@@ -93,6 +93,9 @@ def parse_args(argv=None):
     ap.add_argument("--prefill-ctas", type=int, default=0,
                     help="planner option: SMs of the prefill grid beside the split-KV kernel "
                          "(0: the planner's model, < 0: every SM)")
+    ap.add_argument("--kv-chunk", type=int, default=0,
+                    help="planner option: split-KV chunk in keys (multiple of 64; 0: the "
+                         "planner's choice)")
     ap.add_argument("--layers", type=int, default=1,
                     help="a step runs this many layers, each with its own cache: one plan, "
                          "then append + forward per layer, back to back")
@@ -443,6 +446,8 @@ def workload_config_args(w, args, world=1):
         c["cascade"] = "disabled"
     if args.prefill_ctas:
         c["prefill_ctas"] = args.prefill_ctas
+    if args.kv_chunk:
+        c["kv_chunk"] = args.kv_chunk
     if args.rope:
         c["append"] = "fused rotary embedding + KV append (mb_rope_kv_append)"
         c["step"] = "mb_rope_kv_append + mb_attn_plan (host + 1 H2D) + mb_attn_forward"
@@ -574,9 +579,10 @@ def measure(args, name, dev, local, world, *, main):
         torch.cuda.empty_cache()
     s = w.spec
     opts = None
-    if main and (args.disable_cascade or args.prefill_ctas or fp8):
+    if main and (args.disable_cascade or args.prefill_ctas or args.kv_chunk or fp8):
         opts = B.options(disable_cascade=1 if args.disable_cascade else 0,
-                         prefill_ctas=args.prefill_ctas, fp8_cache=1 if fp8 else 0)
+                         prefill_ctas=args.prefill_ctas, kv_chunk=args.kv_chunk,
+                         fp8_cache=1 if fp8 else 0)
     cfg = B.config(s.n_q_heads, s.n_kv_heads, s.head_dim, s.page_size, w.num_pages,
                    w.block_table.shape[1], s.scale or 0.0)
     shape = (w.num_pages, s.n_kv_heads, s.page_size, s.head_dim)
@@ -942,7 +948,7 @@ def run_gpu(args):
     torch.cuda.empty_cache()
 
     plain = not (args.fp8 or args.rope or args.max_requests or args.disable_cascade
-                 or args.layers > 1 or args.prefill_ctas)
+                 or args.layers > 1 or args.prefill_ctas or args.kv_chunk)
     if args.workload == DEFAULT_WORKLOAD and plain and not args.no_workloads:
         extra = {}
         for name in LINE_WORKLOADS:

@@ -10,6 +10,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <functional>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -51,6 +52,15 @@ constexpr double kHbmGBs = 6600.0;
 // the same two rates for the split-KV kernel over an fp8 cache
 constexpr double kDecodeFp8SmGBs = 26.0;
 constexpr double kHbmFp8GBs = 3950.0;
+// A small split-KV batch beside prefill work is latency-bound: each CTA takes
+// a fixed time (set-up, its first tiles' latency, epilogue) plus a time per
+// 128-key tile that its ring, not HBM, sets; beside it, a prefill item costs
+// more than the tile model above counts (the item's Q load, ramp and
+// epilogue). Fitted to measured steps of the Llama-2-7B-shaped iteration
+// over prefill grids of 120-152 CTAs and two chunkings (rms 4.5 us).
+constexpr double kDecodeCtaUs = 14.0;
+constexpr double kDecodeTileUs = 1.7;
+constexpr double kPrefillItemLatencyUs = 9.0;
 
 bool is_pow2_in(int v, int lo, int hi) {
   return v >= lo && v <= hi && (v & (v - 1)) == 0;
@@ -140,6 +150,37 @@ std::vector<int32_t> heavy_first(size_t n, KeyFn key) {
   return order;
 }
 
+// Modelled cost of each prefill item (us): a fixed cost per item plus its
+// query tiles' KV tiles (one 128-row query tile against one 128-key tile).
+std::vector<double> prefill_costs(const std::vector<PrefillItem>& pitems, int D, double item_us) {
+  const double tile_us = kPrefillTileUs * (D / 16 + 8) / 16.0;
+  std::vector<double> cost(pitems.size());
+  for (size_t i = 0; i < pitems.size(); ++i) {
+    const PrefillItem& p = pitems[i];
+    const int32_t ra = std::min(kPrefillTileM, p.n_rows), rb = std::max(0, p.n_rows - kPrefillTileM);
+    const int32_t na = (std::min(p.kv_length, p.s0 + p.i0 + ra) + kPrefillTileN - 1) / kPrefillTileN;
+    const int32_t nb = rb > 0 ? (std::min(p.kv_length, p.s0 + p.i0 + kPrefillTileM + rb) +
+                                 kPrefillTileN - 1) / kPrefillTileN
+                              : 0;
+    cost[i] = item_us + (na + nb) * tile_us;
+  }
+  return cost;
+}
+
+// Finishing time of each of P prefill CTAs: the items, heavy first, dealt
+// in the kernel's snake order (ascending when `sorted`).
+void prefill_finish(const std::vector<double>& cost, int32_t P, std::vector<double>& load,
+                    bool sorted = true) {
+  const int32_t n = (int32_t)cost.size();
+  load.assign((size_t)P, 0.0);
+  for (int32_t k = 0; k * P < n; ++k)
+    for (int32_t b = 0; b < P; ++b) {
+      const int32_t idx = k * P + ((k & 1) ? P - 1 - b : b);
+      if (idx < n) load[(size_t)b] += cost[(size_t)idx];
+    }
+  if (sorted) std::sort(load.begin(), load.end());
+}
+
 // SMs for the persistent prefill grid when the split-KV kernel runs beside
 // it: the grid P whose modelled step time is least (the largest such P on a
 // tie). The prefill items (heavy first) go to P CTAs in snake order, which
@@ -150,30 +191,12 @@ std::vector<int32_t> heavy_first(size_t n, KeyFn key) {
 int32_t partition_sms(const std::vector<PrefillItem>& pitems, int64_t decode_bytes, int D,
                       double sm_gbs, double full_gbs) {
   const int32_t n = (int32_t)pitems.size();
-  const int32_t hi = std::min<int32_t>(n, kSms);
-  const double tile_us = kPrefillTileUs * (D / 16 + 8) / 16.0;
-  std::vector<double> cost((size_t)n);
-  for (int32_t i = 0; i < n; ++i) {
-    const PrefillItem& p = pitems[(size_t)i];
-    const int32_t ra = std::min(kPrefillTileM, p.n_rows), rb = std::max(0, p.n_rows - kPrefillTileM);
-    const int32_t na = (std::min(p.kv_length, p.s0 + p.i0 + ra) + kPrefillTileN - 1) / kPrefillTileN;
-    const int32_t nb = rb > 0 ? (std::min(p.kv_length, p.s0 + p.i0 + kPrefillTileM + rb) +
-                                 kPrefillTileN - 1) / kPrefillTileN
-                              : 0;
-    cost[(size_t)i] = kPrefillItemUs + (na + nb) * tile_us;
-  }
+  const int32_t hi = std::min<int32_t>(n, kSms), lo = std::max<int32_t>(1, hi / 4);
+  const std::vector<double> cost = prefill_costs(pitems, D, kPrefillItemUs);
   const double bytes_per_us_sm = sm_gbs * 1e3, bytes_per_us_full = full_gbs * 1e3;
-  int32_t best = hi;
-  double best_t = 1e300;
   std::vector<double> load;
-  for (int32_t P = hi; P >= std::max<int32_t>(1, hi / 4); --P) {
-    load.assign((size_t)P, 0.0);
-    for (int32_t k = 0; k * P < n; ++k)
-      for (int32_t b = 0; b < P; ++b) {
-        const int32_t idx = k * P + ((k & 1) ? P - 1 - b : b);
-        if (idx < n) load[(size_t)b] += cost[(size_t)idx];
-      }
-    std::sort(load.begin(), load.end());
+  auto step_of = [&](int32_t P) {
+    prefill_finish(cost, P, load);
     const double t_pre = load.back();
     // walk the intervals between prefill CTAs' finishing times
     double left = (double)decode_bytes, t = 0.0, t_dec = -1.0;
@@ -186,13 +209,78 @@ int32_t partition_sms(const std::vector<PrefillItem>& pitems, int64_t decode_byt
       t = t_next;
       ++free_sms;
     }
+    return std::max(t_pre, t_dec);
+  };
+  // every 4th grid size from the full one down, then every size around the
+  // best of those (the modelled time is nearly smooth in P)
+  int32_t best = hi;
+  double best_t = 1e300;
+  auto consider = [&](int32_t P) {
+    const double st = step_of(P);
+    if (st < best_t * (1.0 - 1e-3) || (st < best_t * (1.0 + 1e-3) && P > best)) {
+      if (st < best_t) best_t = st;
+      best = P;
+    }
+  };
+  for (int32_t P = hi; P >= lo; P -= 4) consider(P);
+  const int32_t c = best;
+  for (int32_t P = std::min(hi, c + 3); P >= std::max(lo, c - 3); --P)
+    if (P != c && (c - P) % 4 != 0) consider(P);
+  return best;
+}
+
+// The same choice for a small (latency-bound) split-KV batch, whose CTAs
+// (tiles[i] 128-key tiles each, heaviest first, the order the hardware hands
+// them out) take kDecodeCtaUs + tiles * kDecodeTileUs each: they go, in
+// order, to the earliest free SM among the kSms - P without a prefill CTA and
+// the prefill SMs as their CTAs finish. The list schedule only changes where
+// ceil(CTAs / free SMs) does, so P is tried there and at the full grid.
+// Returns the modelled step time (us) and the best P in *best_p.
+double latency_partition(const std::vector<double>& cost, const std::vector<int32_t>& tiles,
+                         int32_t* best_p) {
+  const int32_t n = (int32_t)cost.size();
+  const int32_t hi = std::min<int32_t>(n, kSms), lo = std::max<int32_t>(1, hi / 4);
+  const int32_t C = (int32_t)tiles.size();
+  double total = 0.0;
+  for (double c : cost) total += c;
+  const double cta_max = kDecodeCtaUs + (C ? tiles[0] : 0) * kDecodeTileUs;
+  // candidates: the full grid, and of the grids where the CTAs' wave count
+  // on the free SMs changes, the three whose rough estimate (balanced
+  // prefill, whole waves of the longest CTA) is least
+  std::vector<std::pair<double, int32_t>> est;
+  for (int32_t wv = 1; wv <= std::min<int32_t>(C, 64); ++wv) {
+    const int32_t P = kSms - (C + wv - 1) / wv;
+    if (P < lo || P >= hi) continue;
+    const double e = std::max(total / P, wv * cta_max);
+    if (est.empty() || est.back().second != P) est.emplace_back(e, P);
+  }
+  std::sort(est.begin(), est.end());
+  std::vector<int32_t> cand{hi};
+  for (size_t i = 0; i < est.size() && i < 3; ++i) cand.push_back(est[i].second);
+  std::sort(cand.begin(), cand.end(), std::greater<int32_t>());
+  double best_t = 1e300;
+  *best_p = hi;
+  std::vector<double> load;
+  for (int32_t P : cand) {
+    prefill_finish(cost, P, load, false);
+    const double t_pre = *std::max_element(load.begin(), load.end());
+    load.insert(load.end(), (size_t)(kSms - P), 0.0);
+    std::make_heap(load.begin(), load.end(), std::greater<double>());
+    double t_dec = 0.0;
+    for (int32_t t : tiles) {
+      std::pop_heap(load.begin(), load.end(), std::greater<double>());
+      const double e = load.back() + kDecodeCtaUs + t * kDecodeTileUs;
+      load.back() = e;
+      std::push_heap(load.begin(), load.end(), std::greater<double>());
+      t_dec = std::max(t_dec, e);
+    }
     const double step = std::max(t_pre, t_dec);
     if (step < best_t * (1.0 - 1e-3)) {
       best_t = step;
-      best = P;
+      *best_p = P;
     }
   }
-  return best;
+  return best_t;
 }
 
 }  // namespace
@@ -303,6 +391,40 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
     seqs.push_back(sq);
   }
 
+  // ---- prefill items, heaviest first -----------------------------------
+  std::vector<PrefillItem> pitems;
+  {
+    size_t np = 0;
+    for (int32_t r : prefill_reqs)
+      np += (size_t)Hq * ((reqs[r].q_end - reqs[r].q_start + kPrefillCtaRows - 1) / kPrefillCtaRows);
+    pitems.reserve(np);
+  }
+  for (int32_t r : prefill_reqs) {
+    const mb_request_t& q = reqs[r];
+    const int32_t m = q.q_end - q.q_start, s0 = q.kv_length - m;
+    for (int32_t h = 0; h < Hq; ++h)
+      for (int32_t i0 = 0; i0 < m; i0 += kPrefillCtaRows) {
+        PrefillItem p;
+        p.req = r;
+        p.q_head = h;
+        p.q_row0 = q.q_start + i0;
+        p.n_rows = std::min(kPrefillCtaRows, m - i0);
+        p.s0 = s0;
+        p.i0 = i0;
+        p.kv_length = q.kv_length;
+        const int32_t last = std::min(q.kv_length, s0 + i0 + p.n_rows);
+        p.n_kv_tiles = (last + kPrefillTileN - 1) / kPrefillTileN;
+        pitems.push_back(p);
+      }
+  }
+  {
+    const std::vector<int32_t> order =
+        heavy_first(pitems.size(), [&](size_t i) { return pitems[i].n_kv_tiles; });
+    std::vector<PrefillItem> sorted(pitems.size());
+    for (size_t i = 0; i < order.size(); ++i) sorted[i] = pitems[order[i]];
+    pitems.swap(sorted);
+  }
+
   // ---- split-KV chunk size ---------------------------------------------
   int64_t work = 0;   // key-visits summed over CTAs if nothing were split
   int64_t tiles = 0;  // the same in 128-key tiles
@@ -355,6 +477,47 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
     };
     const int step = std::max(ps, 128);
     for (int guard = 0; guard < 4096 && ctas() > kSms; ++guard) chunk += step;
+  }
+  // A small batch beside prefill work: its CTAs are latency-bound, and how
+  // many SMs the prefill grid leaves them decides how long they take, so the
+  // chunk (sized for one wave of SMs, or every key range whole) is chosen
+  // together with the prefill grid's size (latency_partition).
+  int32_t latency_p = 0;
+  if (one_wave && !pitems.empty() && o.prefill_ctas == 0 && !o.fp8_cache) {
+    const std::vector<double> cost = prefill_costs(pitems, D, kPrefillItemLatencyUs);
+    auto cta_tiles = [&]() {
+      std::vector<int32_t> t;
+      for (const Sequence& s : seqs) {
+        const int32_t len = s.k_end - s.k_begin;
+        if (len <= 0) continue;
+        int64_t rs = 0;
+        for (int32_t x = s.mbeg; x < s.mend; ++x) {
+          const int32_t r = member_list[x];
+          rs += (int64_t)(reqs[r].q_end - reqs[r].q_start) * g;
+        }
+        const int64_t ctas = ((rs + kRowsPerDecodeItem - 1) / kRowsPerDecodeItem) * Hkv;
+        const int32_t part = part_of(s), nc = (len + part - 1) / part;
+        for (int32_t c = 0; c < nc; ++c) {
+          const int32_t lc = std::min(part, len - c * part);
+          t.insert(t.end(), (size_t)ctas, (lc + 127) / 128);
+        }
+      }
+      std::sort(t.begin(), t.end(), std::greater<int32_t>());
+      return t;
+    };
+    int32_t p_wave = 0, p_whole = 0;
+    const double t_wave = latency_partition(cost, cta_tiles(), &p_wave);
+    const int32_t chunk_wave = chunk;
+    int32_t longest = 0;
+    for (const Sequence& s : seqs) longest = std::max(longest, s.k_end - s.k_begin);
+    chunk = std::max(chunk_wave, ((longest + ps - 1) / ps) * ps);
+    const double t_whole = latency_partition(cost, cta_tiles(), &p_whole);
+    if (t_whole < t_wave * (1.0 - 1e-3)) {
+      latency_p = p_whole;
+    } else {
+      chunk = chunk_wave;
+      latency_p = p_wave;
+    }
   }
   auto n_chunks = [&](const Sequence& s) -> int32_t {
     const int32_t len = s.k_end - s.k_begin;
@@ -469,40 +632,6 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
     items.swap(sorted);
   }
 
-  // ---- prefill items, heaviest first -----------------------------------
-  std::vector<PrefillItem> pitems;
-  {
-    size_t np = 0;
-    for (int32_t r : prefill_reqs)
-      np += (size_t)Hq * ((reqs[r].q_end - reqs[r].q_start + kPrefillCtaRows - 1) / kPrefillCtaRows);
-    pitems.reserve(np);
-  }
-  for (int32_t r : prefill_reqs) {
-    const mb_request_t& q = reqs[r];
-    const int32_t m = q.q_end - q.q_start, s0 = q.kv_length - m;
-    for (int32_t h = 0; h < Hq; ++h)
-      for (int32_t i0 = 0; i0 < m; i0 += kPrefillCtaRows) {
-        PrefillItem p;
-        p.req = r;
-        p.q_head = h;
-        p.q_row0 = q.q_start + i0;
-        p.n_rows = std::min(kPrefillCtaRows, m - i0);
-        p.s0 = s0;
-        p.i0 = i0;
-        p.kv_length = q.kv_length;
-        const int32_t last = std::min(q.kv_length, s0 + i0 + p.n_rows);
-        p.n_kv_tiles = (last + kPrefillTileN - 1) / kPrefillTileN;
-        pitems.push_back(p);
-      }
-  }
-  {
-    const std::vector<int32_t> order =
-        heavy_first(pitems.size(), [&](size_t i) { return pitems[i].n_kv_tiles; });
-    std::vector<PrefillItem> sorted(pitems.size());
-    for (size_t i = 0; i < order.size(); ++i) sorted[i] = pitems[order[i]];
-    pitems.swap(sorted);
-  }
-
   // ---- split-KV build: row copies when most keys sit in long CTAs of
   // <= 32 rows (see splitkv_kernel) ---------------------------------------
   int32_t decode_copies = 0;
@@ -521,6 +650,8 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
   if (!pitems.empty() && !items.empty()) {
     if (o.prefill_ctas > 0) {
       prefill_ctas = std::min(prefill_ctas, o.prefill_ctas);
+    } else if (o.prefill_ctas == 0 && latency_p > 0) {
+      prefill_ctas = std::min(prefill_ctas, latency_p);
     } else if (o.prefill_ctas == 0) {
       // K and V bytes the split-KV CTAs read (fp8: codes and row scales)
       const int64_t per_key = o.fp8_cache ? 2 * (D + 4) : 4 * D;
