@@ -226,6 +226,25 @@ def test_planner_coverage_options(L, name, opts):
     check_coverage(w, B.options(**opts))
 
 
+def test_small_decode_batch_beside_prefill_gets_sms_and_whole_ranges(L):
+    # two MHA decodes beside a 4096-row prompt: their 64 (request, head) CTAs
+    # are latency-bound, so the planner leaves them SMs next to the prefill
+    # grid and keeps each key range whole (one CTA per request and KV head)
+    # rather than splitting the ranges into one wave of short CTAs after it
+    w = W.make_workload("llama2_7b_orca_iteration", with_values=False)
+    inf = B.HostPlan(w.requests, w.block_table, cfg_for(w)).info
+    assert inf.n_prefill_items == 512 and 0 < inf.prefill_ctas < 152
+    assert inf.n_decode_items == 2 * 32 and inf.n_combine == 0 and inf.n_partials == 0
+    assert inf.kv_chunk >= 1700
+    # every SM to the prefill grid (the caller's choice): one wave of split
+    # CTAs that run in its tail
+    inf = B.HostPlan(w.requests, w.block_table, cfg_for(w), B.options(prefill_ctas=-1)).info
+    assert inf.prefill_ctas == 152 and inf.n_decode_items > 64 and inf.n_combine == 2 * 32
+    # a chunk fixed by the caller is kept
+    inf = B.HostPlan(w.requests, w.block_table, cfg_for(w), B.options(kv_chunk=512)).info
+    assert inf.kv_chunk == 512
+
+
 def test_prefill_tiles_skip_masked_tiles(L):
     # one 4096-row prefill: CTA t owns rows [256 t, 256 t + 256) and visits
     # exactly the 2 t + 2 KV tiles of 128 keys its last row can see
