@@ -57,7 +57,8 @@ constexpr double kHbmFp8GBs = 3950.0;
 // 128-key tile that its ring, not HBM, sets; beside it, a prefill item costs
 // more than the tile model above counts (the item's Q load, ramp and
 // epilogue). Fitted to measured steps of the Llama-2-7B-shaped iteration
-// over prefill grids of 120-152 CTAs and two chunkings (rms 4.5 us).
+// over prefill grids of 120-152 CTAs and two chunkings (rms 4.5 us); the fp8
+// split-KV kernel's short CTAs measured the same (same best grid and chunk).
 constexpr double kDecodeCtaUs = 14.0;
 constexpr double kDecodeTileUs = 1.7;
 constexpr double kPrefillItemLatencyUs = 9.0;
@@ -483,7 +484,7 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
   // chunk (sized for one wave of SMs, or every key range whole) is chosen
   // together with the prefill grid's size (latency_partition).
   int32_t latency_p = 0;
-  if (one_wave && !pitems.empty() && o.prefill_ctas == 0 && !o.fp8_cache) {
+  if (one_wave && !pitems.empty() && o.prefill_ctas == 0) {
     const std::vector<double> cost = prefill_costs(pitems, D, kPrefillItemLatencyUs);
     auto cta_tiles = [&]() {
       std::vector<int32_t> t;
