@@ -114,7 +114,10 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new,
 // row, scale = amax(|row|) / 448, code = e4m3(x / scale) rounded to nearest
 // (ties to even), saturating; a zero row gets scale 0 and zero codes. The
 // quotient is one IEEE fp32 division, so the codes are reproducible.
-// One warp per row: each lane holds D/32 consecutive values.
+// D/8 lanes per row, 8 consecutive values each (one 16-byte load, one
+// 8-byte store of codes), so a warp quantizes 32/(D/8) rows at once and the
+// amax reduction and the per-row address work are shared by fewer values'
+// worth of instructions (the kernel is issue-bound, not bound by HBM).
 namespace mb {
 namespace {
 
@@ -124,11 +127,13 @@ __global__ void __launch_bounds__(128) kv_append_fp8_kernel(
     float* __restrict__ vs, const __nv_bfloat16* __restrict__ kn,
     const __nv_bfloat16* __restrict__ vn, const int32_t* __restrict__ slots, int32_t Hkv,
     int32_t ps_shift, int64_t n_slots, int32_t* status) {
-  constexpr int E = D / 32;  // values per lane (4 for D = 128, 2 for D = 64)
+  constexpr int kL = D / 8;       // lanes per row: 8 values (one 16-byte load) each
+  constexpr int kRpw = 32 / kL;   // rows a warp handles at once
   dev::pdl_launch_dependents();
   dev::pdl_wait();
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane / kL, l = lane % kL;
   const int32_t slot = __ldg(slots + t);
   if (slot < 0) return;
   if ((int64_t)slot >= n_slots) {
@@ -137,39 +142,42 @@ __global__ void __launch_bounds__(128) kv_append_fp8_kernel(
   }
   const int32_t page = slot >> ps_shift;
   const int32_t off = slot & ((1 << ps_shift) - 1);
-  for (int row = warp; row < 2 * Hkv; row += 4) {
-    const int h = row < Hkv ? row : row - Hkv;
-    const __nv_bfloat16* src = (row < Hkv ? kn : vn) + ((int64_t)t * Hkv + h) * D + E * lane;
-    float x[E];
+  const int n_rows = 2 * Hkv;
+  for (int row0 = warp * kRpw; row0 < n_rows; row0 += 4 * kRpw) {
+    const int row = row0 + sub;
+    const bool valid = row < n_rows;
+    const bool is_v = row >= Hkv;
+    const int h = is_v ? row - Hkv : row;
+    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+    if (valid)
+      raw = __ldg(reinterpret_cast<const uint4*>((is_v ? vn : kn) + ((int64_t)t * Hkv + h) * D) + l);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    float x[8];
     float amax = 0.f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      x[e] = __bfloat162float(src[e]);
-      amax = fmaxf(amax, fabsf(x[e]));
+    for (int e = 0; e < 4; ++e) {
+      x[2 * e] = dev::bf16_lo(w[e]);
+      x[2 * e + 1] = dev::bf16_hi(w[e]);
+      amax = dev::fmax3(amax, fabsf(x[2 * e]), fabsf(x[2 * e + 1]));
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    for (int o = kL / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float scale = __fdiv_rn(amax, 448.0f);
-    uint8_t code[E];
-#pragma unroll
-    for (int e = 0; e < E; e += 2) {
-      uint16_t pair = 0;
-      if (scale > 0.f) {
-        const float a = __fdiv_rn(x[e], scale), b = __fdiv_rn(x[e + 1], scale);
-        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(b), "f"(a));
+    uint32_t code[2] = {0u, 0u};
+    if (scale > 0.f) {
+      #pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        uint16_t pair;
+        const float qa = __fdiv_rn(x[e], scale), qb = __fdiv_rn(x[e + 1], scale);
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(qb), "f"(qa));
+        code[e >> 2] |= (uint32_t)pair << (8 * (e & 3));
       }
-      code[e] = (uint8_t)(pair & 0xff);
-      code[e + 1] = (uint8_t)(pair >> 8);
     }
-    const int64_t drow = (((int64_t)page * Hkv + h) << ps_shift) + off;
-    uint8_t* dst = (row < Hkv ? k8 : v8) + drow * D + E * lane;
-    if constexpr (E == 4) {
-      *reinterpret_cast<uint32_t*>(dst) = (uint32_t)code[0] | ((uint32_t)code[1] << 8) |
-                                          ((uint32_t)code[2] << 16) | ((uint32_t)code[3] << 24);
-    } else {
-      *reinterpret_cast<uint16_t*>(dst) = (uint16_t)(code[0] | (code[1] << 8));
+    if (valid) {
+      const int64_t drow = (((int64_t)page * Hkv + h) << ps_shift) + off;
+      *reinterpret_cast<uint2*>((is_v ? v8 : k8) + drow * D + 8 * l) = make_uint2(code[0], code[1]);
+      if (l == 0) (is_v ? vs : ks)[drow] = scale;
     }
-    if (lane == 0) (row < Hkv ? ks : vs)[drow] = scale;
   }
 }
 
