@@ -309,6 +309,37 @@ def test_fp8_chunked_prefill_mix_sampled():
                 np.testing.assert_allclose(ls[qs + a:qs + b, h], l_ref, rtol=TOL, atol=TOL)
 
 
+def test_fp8_long_context_sampled():
+    # the bf16 long-context case on the fp8 cache: a 131072-key decode (128
+    # partials per row with a 1024-key chunk), a 65537-key decode and a
+    # 300-row chunk over a 100k-key history, whose pages are staged for the
+    # tensor-core kernel
+    w = custom_workload([(1, 131072), (300, 100000), (1, 65537)], n_q_heads=8, n_kv_heads=2,
+                        head_dim=128, page_size=64, seed=21)
+    s = w.spec
+    g = s.n_q_heads // s.n_kv_heads
+    for opts in (dict(fp8_cache=1), dict(fp8_cache=1, kv_chunk=1024)):
+        out, lse, status, info = run_fp8(w, opts=opts)
+        assert status == 0 and info["staged_pages"] > 0
+        o = out.to(torch.float64).cpu().numpy()
+        ls = lse.to(torch.float64).cpu().numpy()
+        for r, rows, heads in ((0, [(0, 1)], range(8)), (2, [(0, 1)], range(8)),
+                               (1, [(0, 16), (284, 300)], (0, 5))):
+            qs, qe, kv = [int(x) for x in w.requests[r]]
+            k, v = w.logical_kv(r)
+            kd = F.dequantize_rows(*F.quantize_rows(k.float().cpu().numpy()))
+            vd = F.dequantize_rows(*F.quantize_rows(v.float().cpu().numpy()))
+            m = qe - qs
+            for a, b in rows:
+                q = w.q[qs + a:qs + b].to(torch.float64).cpu().numpy()
+                for h in heads:
+                    o_ref, l_ref = _attend_rows(q[:, h], kd[:, h // g], vd[:, h // g], kv - m + a,
+                                                s.scale)
+                    np.testing.assert_allclose(o[qs + a:qs + b, h], o_ref, rtol=TOL, atol=TOL,
+                                               err_msg=f"request {r} head {h} rows {a}:{b}")
+                    np.testing.assert_allclose(ls[qs + a:qs + b, h], l_ref, rtol=TOL, atol=TOL)
+
+
 def _attend_rows(q, k, v, first_pos, scale):
     """fp64 attention of query rows q [n, D] at positions first_pos..first_pos
     + n - 1 over keys k, v [>= first_pos + n, D] (row i sees keys <= its

@@ -199,6 +199,25 @@ def test_edge_cases(case, opt):
             assert_request_close(w, out, lse, r)
 
 
+def test_long_context_many_partials():
+    # the largest ranges of any test: a 131072-key decode (with a 1024-key
+    # chunk: 128 partials per row, which the in-kernel merge reads 16 slots
+    # at a time), a 65537-key decode, and a 300-row chunk over a 100k-key
+    # history (sampled rows and heads); the default plan and the forced split
+    w = custom_workload([(1, 131072), (300, 100000), (1, 65537)], n_q_heads=8, n_kv_heads=2,
+                        head_dim=128, page_size=64, seed=21)
+    kc, vc, cfg = fill_cache(w)
+    for opts in (None, B.options(kv_chunk=1024)):
+        out, lse, status, info = run_forward(w, kc, vc, cfg, opts)
+        assert status == 0
+        if opts is not None:
+            assert info["n_partials"] >= 128 * 8 + 65 * 8
+        assert_request_close(w, out, lse, 0)
+        assert_request_close(w, out, lse, 2)
+        for rows in [(0, 16), (284, 300)]:
+            assert_request_close(w, out, lse, 1, heads=[0, 5], rows=rows)
+
+
 # Long key ranges (>= 16 tiles of 128 keys per split-KV CTA). A plan with
 # most of its keys in such CTAs of <= 32 rows runs the split-KV build that
 # spreads each row's keys over 4 copies in the softmax warps; its CTAs with
