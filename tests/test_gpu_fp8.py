@@ -309,6 +309,18 @@ def test_fp8_chunked_prefill_mix_sampled():
                 np.testing.assert_allclose(ls[qs + a:qs + b, h], l_ref, rtol=TOL, atol=TOL)
 
 
+def test_fp8_a_thousand_short_requests():
+    # 1000 short requests of every kind on the fp8 cache (decode work on the
+    # codes, the chunks' pages staged for the tensor-core kernel)
+    rng = np.random.default_rng(34)
+    shapes = [(1, 1)] + [((1, 4, 24)[i % 3], 0) for i in range(999)]
+    shapes = [(m, kv if kv else int(rng.integers(m, 301))) for m, kv in shapes]
+    w = custom_workload(shapes, n_q_heads=8, n_kv_heads=2, head_dim=128, page_size=16, seed=34)
+    out, lse, status, info = run_fp8(w, opts=dict(fp8_cache=1))
+    assert status == 0 and info["staged_pages"] > 0
+    check_all(w, out, lse)
+
+
 def test_fp8_long_context_sampled():
     # the bf16 long-context case on the fp8 cache: a 131072-key decode (128
     # partials per row with a 1024-key chunk), a 65537-key decode and a

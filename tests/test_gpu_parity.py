@@ -199,6 +199,29 @@ def test_edge_cases(case, opt):
             assert_request_close(w, out, lse, r)
 
 
+def test_a_thousand_short_requests():
+    # the most requests of any test: 1000 requests of every kind but long
+    # (decodes at kv 1..300, 4-row speculative steps, 24-row chunks), so the
+    # plan has thousands of short split-KV CTAs and prefill items; every
+    # request checked in full
+    rng = np.random.default_rng(33)
+    shapes = [(1, 1), (1, 16)]
+    for i in range(998):
+        kind = i % 3
+        if kind == 0:
+            shapes.append((1, int(rng.integers(1, 301))))
+        elif kind == 1:
+            shapes.append((4, int(rng.integers(4, 301))))
+        else:
+            shapes.append((24, int(rng.integers(24, 301))))
+    w = custom_workload(shapes, n_q_heads=8, n_kv_heads=2, head_dim=128, page_size=16, seed=33)
+    kc, vc, cfg = fill_cache(w)
+    out, lse, status, info = run_forward(w, kc, vc, cfg)
+    assert status == 0 and info["n_prefill_items"] > 0 and info["n_decode_items"] > 600
+    for r in range(w.n_requests):
+        assert_request_close(w, out, lse, r)
+
+
 def test_long_context_many_partials():
     # the largest ranges of any test: a 131072-key decode (with a 1024-key
     # chunk: 128 partials per row, which the in-kernel merge reads 16 slots
