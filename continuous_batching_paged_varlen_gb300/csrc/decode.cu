@@ -19,12 +19,16 @@
 // This path is bound by HBM bandwidth, so the design spends everything on
 // keeping bytes in flight and almost nothing on issue slots:
 //   warp 4      TMA producer: K_j, V_j, K_j+1, ... page by page through the
-//               block table into a 6-slot ring (one box per page and 64-column
-//               block, one lane per box), 128-byte swizzle.
+//               block table into a 7-slot ring (one box per page and 64-column
+//               block, one lane per box), 128-byte swizzle. The ring takes all
+//               of shared memory: the query rows live in TMEM, so a CTA whose
+//               rate is set by its bytes in flight (beside the prefill kernel,
+//               or with few rows) streams a seventh faster than with 6 slots.
 //   warp 5      TMEM allocation; one lane issues S = Q K^T (M 128 = the
-//               gathered rows, N 128 keys, K = D) into a double-buffered TMEM
-//               tile and O += P V (P from TMEM, V from shared memory). The
-//               tensor core is mostly idle: it only spares the CUDA cores.
+//               gathered rows from TMEM, N 128 keys, K = D) into a
+//               double-buffered TMEM tile and O += P V (P from TMEM, V from
+//               shared memory). The tensor core is mostly idle: it only
+//               spares the CUDA cores.
 //   warps 0-3   softmax: TMEM load of a row's scores, mask, online max / sum
 //               in the log2 domain, P back into TMEM over the scores, rare O
 //               rescale, epilogue. One thread per query row (only warps that
@@ -63,12 +67,13 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // + 128 * buffer
 constexpr uint32_t kColO = 256;
+constexpr uint32_t kColQ = 384;  // the query rows, bf16 pairs (D / 2 columns)
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint64_t kDrainNs = 200000000ull;
 
 enum {
-  kSlots = 6,
+  kSlots = 7,
   B_KV_FULL = 0,              // + slot
   B_KV_EMPTY = kSlots,        // + slot
   B_S_FULL = 2 * kSlots,      // + buffer
@@ -88,8 +93,7 @@ struct Layout {
   static constexpr int kHalves = D / 64;
   static constexpr uint32_t kHalfBytes = 128 * 128;
   static constexpr uint32_t kTileBytes = kHalves * kHalfBytes;
-  static constexpr uint32_t q_off = 0;
-  static constexpr uint32_t kv_off = kTileBytes;
+  static constexpr uint32_t kv_off = 0;
   static constexpr uint32_t bar_off = kv_off + kSlots * kTileBytes;
   static constexpr uint32_t misc_off = bar_off + B_COUNT * 8;
   static constexpr uint32_t kBytes = misc_off + 16;
@@ -373,7 +377,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sq = smem + L::q_off;
   uint8_t* skv = smem + L::kv_off;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
@@ -451,45 +454,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_alloc(tmem_slot, kTmemCols);
       tmem_relinquish();
     }
-    // gather the item's query rows into the K-major 128-byte-swizzled Q tile
-    // (rows past n_rows are zero): warps 0-3 and 5, every load in flight
-    // before the producer is released, then the stores
+    // the item's query rows go to TMEM, where the S MMA reads its A operand:
+    // softmax warp w writes tile rows 32 w .. 32 w + 31 into its own lanes,
+    // tile row t holding item row 32 ((t / 32) % ngrp) + t % 32 (each row
+    // once per copy; rows past n_rows zero). The loads are in flight before
+    // the producer is released, the stores follow once TMEM is allocated.
     // q may be the kernel ahead's output (a rotary append rewrites it)
     if (dep_wait) pdl_wait();
-    const uint4* q = static_cast<const uint4*>(a.q);
     constexpr int CH = D / 8;  // 16-byte chunks per row
-    constexpr int kGather = kThreads - 32;
-    constexpr int kPer = (BM * CH + kGather - 1) / kGather;
-    const int gt = threadIdx.x < 128 ? (int)threadIdx.x : (int)threadIdx.x - 32;
-    uint4 qv[kPer];
+    uint4 qv[CH];
+    if (warp < 4) {
+      const uint4* q = static_cast<const uint4*>(a.q);
+      const bool qrow = my_row < nr;
+      const RowDesc qd = qrow ? a.rows[it.row_begin + my_row] : rd;
+      const uint4* src = q + ((int64_t)qd.q_index * a.n_q_heads + qd.q_head) * CH;
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      // tile row t holds item row 32 ((t / 32) % ngrp) + t % 32: each row
-      // once per copy
-      const int idx = gt + k * kGather;
-      const int t = idx / CH, c = idx - t * CH;
-      const int r = ((t >> 5) % ngrp) * 32 + (t & 31);
-      qv[k] = make_uint4(0u, 0u, 0u, 0u);
-      if (idx < BM * CH && r < nr) {
-        const RowDesc qd = a.rows[it.row_begin + r];
-        qv[k] = __ldg(q + ((int64_t)qd.q_index * a.n_q_heads + qd.q_head) * CH + c);
-      }
+      for (int c = 0; c < CH; ++c) qv[c] = qrow ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
     }
     named_barrier_arrive(2, kThreads);  // the producer's wait below
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int idx = gt + k * kGather;
-      const int r = idx / CH, c = idx - r * CH;
-      const int half = c >> 3, c8 = c & 7;
-      if (idx < BM * CH)
-        *reinterpret_cast<uint4*>(sq + half * L::kHalfBytes + r * 128 + ((c8 ^ (r & 7)) << 4)) =
-            qv[k];
-    }
-    fence_proxy_async_smem();
     tc_fence_before();
     named_barrier_sync(1, kThreads - 32);
     tc_fence_after();
     tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    if (warp < 4) {
+      const uint32_t qcol = tmem + ((uint32_t)(warp * 32) << 16) + kColQ;
+#pragma unroll
+      for (int h = 0; h < CH / 8; ++h)
+        tmem_st32(qcol + 32 * h, *reinterpret_cast<const uint32_t(*)[32]>(&qv[8 * h]));
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    named_barrier_sync(3, kThreads - 32);  // Q in TMEM before the first S MMA
+    tc_fence_after();
   }
 
   if (warp == 4) {
@@ -579,7 +575,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
-      const uint32_t qa = smem_u32(sq);
       const uint32_t kva = smem_u32(skv);
       int last_pv = -1;
       auto wait = [&](int b, uint32_t parity) -> bool {
@@ -594,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-          umma_bf16_ss(tmem + kColS + 128 * (j & 1), sdesc_sw128(qa + off, 16, 1024),
+          umma_bf16_ts(tmem + kColS + 128 * (j & 1), tmem + kColQ + kk * 8,
                        sdesc_sw128(k0 + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
         }
         umma_commit(&bars[B_S_FULL + (j & 1)]);
@@ -654,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // one arrival per split row (also after an abort: the counters must stay
     // in step for the next launch); the CTA whose arrival completes a row
     // merges it. Every partial write of this CTA was fenced before the
-    // barrier above. Scratch: the Q tile, no longer read.
+    // barrier above. Scratch: the K/V ring, every copy landed and read.
     dev::MergeArgs mg;
     mg.rows = a.rows + it.row_begin;
     mg.refs = a.row_merge + it.row_begin;
@@ -665,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mg.n_q_heads = a.n_q_heads;
     mg.out = static_cast<__nv_bfloat16*>(a.out);
     mg.lse = a.lse;
-    dev::merge_completed_rows<D, kThreads>(mg, reinterpret_cast<uint32_t*>(sq), true, my_ref,
+    dev::merge_completed_rows<D, kThreads>(mg, reinterpret_cast<uint32_t*>(skv), true, my_ref,
                                            my_out_row);
   }
   if (!dep_wait && threadIdx.x == 0) {
