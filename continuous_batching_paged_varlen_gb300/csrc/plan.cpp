@@ -47,7 +47,7 @@ constexpr int kMinSmallChunk = 256;
 // rate the split-KV kernel reaches on the whole GPU.
 constexpr double kPrefillTileUs = 0.85;
 constexpr double kPrefillItemUs = 2.0;
-constexpr double kDecodeSmGBs = 65.0;
+constexpr double kDecodeSmGBs = 60.0;
 constexpr double kHbmGBs = 6600.0;
 // the same two rates for the split-KV kernel over an fp8 cache
 constexpr double kDecodeFp8SmGBs = 26.0;
