@@ -659,11 +659,16 @@ def measure(args, name, dev, local, world, *, main):
             append_rows(c, k_new, v_new, slots)
 
     def step():
+        # returns the host time of mb_attn_plan (planning and the one upload
+        # enqueued), which the line reports on its own
+        t0 = time.perf_counter()
         plan = B.Plan(w.requests, w.block_table, cfg, device=dev, workspace=ws, opts=opts)
+        t_plan = time.perf_counter() - t0
         for c in caches:
             append(c)
             forward(plan, c, q)
         plan.close()
+        return t_plan
 
     def kernel_pass(stage_events, append_events):
         # the first layer's launches with per-stage events (stages back to
@@ -710,12 +715,14 @@ def measure(args, name, dev, local, world, *, main):
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     host_s = 0.0
+    plan_s = []
     for i in range(K):
         flush()
         ev[i][0].record(stream)
         h0 = time.perf_counter()
-        step()
+        t_plan = step()
         host_s += time.perf_counter() - h0
+        plan_s.append(t_plan)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -761,6 +768,7 @@ def measure(args, name, dev, local, world, *, main):
     res = {"w": w, "info": info, "stage_ms": stage_ms, "ms_step": ms_step, "value": value,
            "total_ms": total_ms, "roof": roof, "work": work, "clk": clk,
            "dev_status": dev_status, "wall": wall, "host_s": host_s,
+           "plan_us": statistics.median(plan_s) * 1e6,
            "launches": launches_per_step * K, "layers": L, "peaks": peaks,
            "combined": combined_bound(work, ms_step, peaks, L)}
 
@@ -891,7 +899,8 @@ def workload_summary(r):
                          "prefill_flops": r["work"]["prefill_flops"]},
          "plan": {k: r["info"][k] for k in ("n_decode_items", "n_prefill_items", "n_combine",
                                             "n_cascade_groups", "cascade_keys", "kv_chunk")},
-         "clocks": r["clk"], "device_status": r["dev_status"], "gpu_launches": r["launches"]}
+         "clocks": r["clk"], "device_status": r["dev_status"], "gpu_launches": r["launches"],
+         "plan_host_us": r["plan_us"]}
     if s.shared_prefix:
         stored = C.distinct_kv_positions(w.requests, w.block_table, s.page_size)
         naive = C.naive_kv_positions(w.requests)
@@ -941,6 +950,7 @@ def run_gpu(args):
         # the Python binding); a step shorter than this on the device is
         # host-bound, the GPU waiting for its launches
         "host_enqueue_us_per_step": r["host_s"] / args.steps * 1e6,
+        "plan_host_us": r["plan_us"],
     }
     dev_status = r["dev_status"]
     cpu_w = w
