@@ -102,7 +102,8 @@ def bits(a):
 
 # ------------------------------------------------------------------ append
 
-@pytest.mark.parametrize("name", ["tiny_mixed", "shared_prefix_decode"])
+@pytest.mark.parametrize("name", ["tiny_mixed", "shared_prefix_decode",
+                                  "llama2_7b_orca_iteration"])
 def test_fp8_append_bit_exact(name):
     w = W.make_workload(name)
     k8, v8, ks, vs, _ = fill_fp8(w)
@@ -280,6 +281,26 @@ def test_fp8_prefill_on_tensor_cores_matches_oracle(case):
              for b in range(-(-int(w.requests[r, 2]) // ps))}
     assert info["staged_pages"] == len(pages)
     check_all(w, out, lse)
+
+
+@pytest.mark.parametrize("name", ["decode_heavy_gqa4", "spec_decode_k3"])
+def test_fp8_decode_batches_sampled(name):
+    # the full decode batches the bench times on the fp8 cache (the planner's
+    # own options), sampled requests against the oracle over its dequantized
+    # K/V
+    w = W.make_workload(name, device="cuda")
+    out, lse, status, info = run_fp8(w, opts=dict(fp8_cache=1))
+    assert status == 0 and info["n_prefill_items"] == 0
+    o = out.to(torch.float64).cpu().numpy()
+    ls = lse.to(torch.float64).cpu().numpy()
+    assert np.isfinite(o).all()
+    rng = np.random.default_rng(5)
+    for r in sorted(rng.choice(w.n_requests, 10, replace=False).tolist()) + [0, w.n_requests - 1]:
+        qs, qe, _ = [int(x) for x in w.requests[r]]
+        o_ref, l_ref = oracle_fp8_request(w, r)
+        np.testing.assert_allclose(o[qs:qe], o_ref, rtol=TOL, atol=TOL, err_msg=f"request {r}")
+        np.testing.assert_allclose(ls[qs:qe], l_ref, rtol=TOL, atol=TOL,
+                                   err_msg=f"lse request {r}")
 
 
 def test_fp8_chunked_prefill_mix_sampled():
