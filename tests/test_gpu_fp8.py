@@ -283,7 +283,7 @@ def test_fp8_prefill_on_tensor_cores_matches_oracle(case):
     check_all(w, out, lse)
 
 
-@pytest.mark.parametrize("name", ["decode_heavy_gqa4", "spec_decode_k3"])
+@pytest.mark.parametrize("name", ["decode_heavy_gqa4", "spec_decode_k3", "shared_prefix_decode"])
 def test_fp8_decode_batches_sampled(name):
     # the full decode batches the bench times on the fp8 cache (the planner's
     # own options), sampled requests against the oracle over its dequantized
@@ -295,7 +295,8 @@ def test_fp8_decode_batches_sampled(name):
     ls = lse.to(torch.float64).cpu().numpy()
     assert np.isfinite(o).all()
     rng = np.random.default_rng(5)
-    for r in sorted(rng.choice(w.n_requests, 10, replace=False).tolist()) + [0, w.n_requests - 1]:
+    k = min(10, w.n_requests)
+    for r in sorted(set(rng.choice(w.n_requests, k, replace=False).tolist()) | {0, w.n_requests - 1}):
         qs, qe, _ = [int(x) for x in w.requests[r]]
         o_ref, l_ref = oracle_fp8_request(w, r)
         np.testing.assert_allclose(o[qs:qe], o_ref, rtol=TOL, atol=TOL, err_msg=f"request {r}")
@@ -303,17 +304,20 @@ def test_fp8_decode_batches_sampled(name):
                                    err_msg=f"lse request {r}")
 
 
-def test_fp8_chunked_prefill_mix_sampled():
-    # the full chunk (2048 rows at kv 32768) on the tensor-core kernel and
-    # the 64 decodes beside it; sampled heads / rows against the oracle
-    w = W.make_workload("chunked_prefill_mix")
+@pytest.mark.parametrize("name,reqs", [("chunked_prefill_mix", (0, 1, 40, 64)),
+                                       ("llama2_7b_orca_iteration", (0, 1, 2))])
+def test_fp8_prefill_batches_sampled(name, reqs):
+    # the full chunk (2048 rows at kv 32768) or prompt (4096 rows) on the
+    # tensor-core kernel over staged pages and the decodes beside it; sampled
+    # heads / rows against the oracle
+    w = W.make_workload(name)
     out, lse, status, info = run_fp8(w, opts=dict(fp8_cache=1))
     assert status == 0 and info["n_prefill_items"] > 0 and info["n_decode_items"] > 0
     s = w.spec
     g = s.n_q_heads // s.n_kv_heads
     o = out.to(torch.float64).cpu().numpy()
     ls = lse.to(torch.float64).cpu().numpy()
-    for r in (0, 1, 40, 64):
+    for r in reqs:
         qs, qe, kv = [int(x) for x in w.requests[r]]
         k, v = w.logical_kv(r)
         kd = F.dequantize_rows(*F.quantize_rows(k.float().cpu().numpy()))
