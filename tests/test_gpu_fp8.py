@@ -305,14 +305,15 @@ def test_fp8_decode_batches_sampled(name):
 
 
 @pytest.mark.parametrize("name,reqs", [("chunked_prefill_mix", (0, 1, 40, 64)),
-                                       ("llama2_7b_orca_iteration", (0, 1, 2))])
+                                       ("llama2_7b_orca_iteration", (0, 1, 2)),
+                                       ("varlen_prefill", (0, 5, 11, 15))])
 def test_fp8_prefill_batches_sampled(name, reqs):
     # the full chunk (2048 rows at kv 32768) or prompt (4096 rows) on the
     # tensor-core kernel over staged pages and the decodes beside it; sampled
     # heads / rows against the oracle
     w = W.make_workload(name)
     out, lse, status, info = run_fp8(w, opts=dict(fp8_cache=1))
-    assert status == 0 and info["n_prefill_items"] > 0 and info["n_decode_items"] > 0
+    assert status == 0 and info["n_prefill_items"] > 0 and info["staged_pages"] > 0
     s = w.spec
     g = s.n_q_heads // s.n_kv_heads
     o = out.to(torch.float64).cpu().numpy()
