@@ -37,7 +37,7 @@ constexpr int kRowsPerDecodeItem = 128; // query rows one split-KV CTA owns (TME
 constexpr int kPrefillTileM = 128;      // query rows per prefill tile (one TMEM accumulator)
 constexpr int kPrefillTileN = 128;      // keys per prefill KV tile
 constexpr int kPrefillCtaRows = 256;    // query rows per prefill CTA (two tiles)
-constexpr int kCopyMinTiles = 16;       // 128-key tiles from which a split-KV CTA of <= 32
+constexpr int kCopyMinTiles = 8;        // 128-key tiles from which a split-KV CTA of <= 32
                                         // rows spreads each row's keys over 4 copies
 
 // One CTA of the split-KV kernel: query rows (all of one KV head) against

@@ -137,7 +137,7 @@ typedef struct {
                                 the prefill kernel per forward              */
   int32_t splitkv_copies;    /* 1: the split-KV build that spreads each row's
                                 keys over copies in the softmax warps (most
-                                keys in CTAs of <= 32 rows and >= 16 tiles) */
+                                keys in CTAs of <= 32 rows and >= 8 tiles) */
 } mb_plan_info_t;
 
 typedef struct mb_plan mb_plan_t;

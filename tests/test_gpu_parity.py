@@ -241,7 +241,7 @@ def test_long_context_many_partials():
             assert_request_close(w, out, lse, 1, heads=[0, 5], rows=rows)
 
 
-# Long key ranges (>= 16 tiles of 128 keys per split-KV CTA). A plan with
+# Long key ranges (>= 8 tiles of 128 keys per split-KV CTA). A plan with
 # most of its keys in such CTAs of <= 32 rows runs the split-KV build that
 # spreads each row's keys over 4 copies in the softmax warps; its CTAs with
 # more rows or short ranges keep one thread per row. Cases: copies alone,
@@ -260,6 +260,12 @@ COPY_CASES = {
     "copies_with_a_40_row_cta": ([(1, 6000), (10, 5000), (1, 7000)],
                                  dict(n_q_heads=8, n_kv_heads=2, head_dim=64, page_size=32),
                                  dict(kv_chunk=8192, prefill_min_rows=-1), 1),
+    "1_row_ctas_of_10_to_15_tiles_copies": ([(1, 1200), (1, 1900), (1, 1500)],
+                                            dict(n_q_heads=4, n_kv_heads=4, head_dim=128,
+                                                 page_size=16), dict(kv_chunk=2048), 1),
+    "short_ranges_one_per_thread": ([(1, 600), (1, 500), (2, 520)],
+                                    dict(n_q_heads=8, n_kv_heads=2, head_dim=128,
+                                         page_size=64), dict(kv_chunk=1024), 0),
     "48_rows_one_per_thread": ([(12, 4000)], dict(n_q_heads=8, n_kv_heads=2, head_dim=128,
                                                   page_size=64),
                                dict(kv_chunk=8192, prefill_min_rows=-1), 0),
