@@ -60,7 +60,7 @@ class PlanInfo(ctypes.Structure):
                 ("total_q", ctypes.c_int32), ("n_launches", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_size_t), ("metadata_bytes", ctypes.c_size_t),
                 ("prefill_ctas", ctypes.c_int32), ("staged_pages", ctypes.c_int32),
-                ("splitkv_copies", ctypes.c_int32)]
+                ("splitkv_copies", ctypes.c_int32), ("splitkv_max_rows", ctypes.c_int32)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

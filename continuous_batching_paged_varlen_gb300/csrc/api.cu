@@ -200,6 +200,7 @@ mb_status_t mb_attn_forward_fp8_timed(const mb_plan_t* plan, const void* q,
       return MB_ERR_CUDA;
     DecodeFp8Args a;
     a.k_map = &km;
+    a.max_rows = d.decode_max_rows;
     a.items = reinterpret_cast<const DecodeItem*>(ws + d.off_decode_items);
     a.rows = reinterpret_cast<const RowDesc*>(ws + d.off_rows);
     a.n_items = d.n_decode_items;

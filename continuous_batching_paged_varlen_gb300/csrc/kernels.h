@@ -121,6 +121,7 @@ struct DecodeFp8Args {
   int32_t after_prefill;      // as in DecodeArgs (the fp8 kernel is launched
   int32_t* done_counter;      // behind the prefill only, never behind an append)
   const CUtensorMap* k_map;  // uint8 codes [rows, D], box D x ps, swizzled (host copy)
+  int32_t max_rows;          // largest n_rows of the items (<= 8 with D = 128: few-row form)
 };
 cudaError_t launch_decode_fp8(const DecodeFp8Args& a, cudaStream_t s, bool overlap_previous = false);
 

@@ -102,6 +102,7 @@ struct PlanDevice {
   int32_t total_q;
   int32_t prefill_ctas;  // prefill grid when the split-KV kernel runs beside it
   int32_t decode_copies;  // split-KV build with row copies (most keys in long CTAs of <= 32 rows)
+  int32_t decode_max_rows;  // largest n_rows of the split-KV CTAs
   float scale;
   size_t off_decode_items, off_rows, off_prefill_items, off_combine, off_row_merge,
       off_combine_count, off_part_lse, off_part_o;

@@ -635,10 +635,11 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
 
   // ---- split-KV build: row copies when most keys sit in long CTAs of
   // <= 32 rows (see splitkv_kernel) ---------------------------------------
-  int32_t decode_copies = 0;
+  int32_t decode_copies = 0, decode_max_rows = 0;
   {
     int64_t long_tiles = 0, all_tiles = 0;
     for (const DecodeItem& it : items) {
+      decode_max_rows = std::max(decode_max_rows, it.n_rows);
       const int64_t t = (it.k_end - it.k_begin + 127) / 128;
       all_tiles += t;
       if (t >= kCopyMinTiles && it.n_rows <= 32) long_tiles += t;
@@ -703,6 +704,7 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
   d.total_q = total_q;
   d.prefill_ctas = pitems.empty() ? 0 : prefill_ctas;
   d.decode_copies = decode_copies;
+  d.decode_max_rows = decode_max_rows;
   d.scale = cfg->scale > 0.f ? cfg->scale : 1.0f / sqrtf((float)D);
   size_t off = kStatusBytes;
   d.off_decode_items = off;
@@ -782,6 +784,7 @@ mb_status_t build_plan(const mb_request_t* reqs, int32_t n,
   info.prefill_ctas = d.prefill_ctas;
   info.staged_pages = d.n_stage_pages;
   info.splitkv_copies = d.decode_copies;
+  info.splitkv_max_rows = d.decode_max_rows;
   return MB_OK;
 }
 

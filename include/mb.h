@@ -138,6 +138,9 @@ typedef struct {
   int32_t splitkv_copies;    /* 1: the split-KV build that spreads each row's
                                 keys over copies in the softmax warps (most
                                 keys in CTAs of <= 32 rows and >= 8 tiles) */
+  int32_t splitkv_max_rows;  /* largest query-row count of a split-KV CTA; an
+                                fp8 cache with head_dim 128 runs the few-row
+                                form of its split-KV kernel when <= 8        */
 } mb_plan_info_t;
 
 typedef struct mb_plan mb_plan_t;
