@@ -759,7 +759,9 @@ def measure(args, name, dev, local, world, *, main):
                                                    s.head_dim)
     names = {"prefill": ("dequant_pages_kernel + prefill_kernel (tcgen05)" if fp8 else
                          "prefill_kernel (tcgen05)"),
-             "decode": "splitkv_fp8_kernel" if fp8 else "splitkv_kernel",
+             "decode": (("splitkv_fp8t_kernel (few-row form)"
+                         if s.head_dim == 128 and 0 < info.get("splitkv_max_rows", 0) <= 8
+                         else "splitkv_fp8_kernel") if fp8 else "splitkv_kernel"),
              "append": ("rope_append_kernel" if rope else
                         "kv_append_fp8_kernel" if fp8 else "kv_append_kernel")}
     dominant = max(stage_ms, key=stage_ms.get) if stage_ms else None
