@@ -146,6 +146,8 @@ def check_coverage(w, opts=None):
     s = w.spec
     g = s.n_q_heads // s.n_kv_heads
     ps = s.page_size
+    # the largest split-KV CTA, which picks the fp8 kernel's form
+    assert inf.splitkv_max_rows == (int(items["n_rows"].max()) if len(items) else 0)
     covered = {}     # (q_index, q_head) -> list of (k_begin, k_end, slot)
     for it in items:
         assert 1 <= it["n_rows"] <= 128
@@ -243,6 +245,17 @@ def test_small_decode_batch_beside_prefill_gets_sms_and_whole_ranges(L):
     # a chunk fixed by the caller is kept
     inf = B.HostPlan(w.requests, w.block_table, cfg_for(w), B.options(kv_chunk=512)).info
     assert inf.kv_chunk == 512
+
+
+@pytest.mark.parametrize("name,rows", [("decode_heavy_gqa4", 4), ("spec_decode_k3", 16),
+                                       ("shared_prefix_decode", 24),
+                                       ("llama2_7b_orca_iteration", 1)])
+def test_plan_reports_largest_splitkv_cta(L, name, rows):
+    # the rows of one split-KV CTA: a decode's g = 4 query heads; a speculative
+    # step's (k + 1) g; the 6 sharers x g of a cascade group; one MHA decode row
+    w = W.make_workload(name, with_values=False)
+    inf = B.HostPlan(w.requests, w.block_table, cfg_for(w)).info
+    assert inf.splitkv_max_rows == rows
 
 
 def test_prefill_tiles_skip_masked_tiles(L):
