@@ -248,8 +248,12 @@ mb_status_t mb_kv_append_fp8(void* k_codes, void* v_codes, float* k_scale, float
  *     the codes directly: Q K^T on the tensor cores in e4m3 (each query row
  *     written once as two e4m3 rows sq (hi + lo), sq = amax|q| / 448, which
  *     keeps q to about 2^-8 of each value), the K scales applied to the
- *     scores, P V on f16 operands (V' = code * v_scale / rho, rho a power of
- *     two bounding the CTA's V scales), fp32 accumulation.
+ *     scores, P V on f16 operands with the V scale and 1 / rho carried by
+ *     V' (V' = code * v_scale / rho) or, when every split-KV CTA holds at
+ *     most 8 rows and head_dim is 128, by P (P' = p * v_scale / rho, V' =
+ *     code), rho a power of two bounding the CTA's V scales; fp32
+ *     accumulation. The two forms differ only in where the f16 roundings
+ *     fall.
  *   - Prefill work needs a plan built with mb_plan_options_t.fp8_cache = 1
  *     (else MB_ERR_UNSUPPORTED, nothing enqueued). Each forward first
  *     dequantizes the pages the prefill requests read (decode(code) * scale
