@@ -16,6 +16,7 @@ import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmb.so")
+ABI_VERSION = 3  # MB_ABI_VERSION of include/mb.h the structures below mirror
 
 MB_OK = 0
 STATUS_NAMES = {0: "MB_OK", 1: "MB_ERR_INVALID_ARG", 2: "MB_ERR_SHAPE",
@@ -100,6 +101,9 @@ def lib():
             "`python -c 'import __graft_entry__ as g; g.build()'` (there is no fallback path)")
     L = ctypes.CDLL(LIB_PATH)
     L.mb_abi_version.restype = _i32
+    if L.mb_abi_version() != ABI_VERSION:
+        raise RuntimeError(f"{LIB_PATH} has ABI version {L.mb_abi_version()}, the binding "
+                           f"expects {ABI_VERSION}: rebuild it")
     L.mb_status_string.restype = ctypes.c_char_p
     L.mb_status_string.argtypes = [ctypes.c_int]
     L.mb_slot_mapping.restype = ctypes.c_int

@@ -58,7 +58,9 @@
 extern "C" {
 #endif
 
-#define MB_ABI_VERSION 2
+/* Bumped whenever a struct or signature below changes (3: mb_plan_info_t
+ * gained splitkv_max_rows). */
+#define MB_ABI_VERSION 3
 
 typedef enum {
   MB_OK = 0,

@@ -44,7 +44,7 @@ def test_exports_every_declared_symbol(L):
     assert {"mb_kv_append", "mb_attn_plan", "mb_attn_forward", "mb_attn_destroy"} <= set(names)
     for n in names:
         assert hasattr(L, n), n
-    assert L.mb_abi_version() == 2
+    assert L.mb_abi_version() == 3
     assert L.mb_status_string(0) == b"ok"
 
 
