@@ -247,6 +247,35 @@ def test_small_decode_batch_beside_prefill_gets_sms_and_whole_ranges(L):
     assert inf.kv_chunk == 512
 
 
+def _host_info(shapes, opts, **kw):
+    spec = W.WorkloadSpec(name="custom", requests=tuple(shapes), seed=0, **kw)
+    blocks = sum(math.ceil(kv / kw["page_size"]) for _, kv in shapes)
+    w = W.make_workload(W.WorkloadSpec(**{**spec.__dict__, "pool_pages": blocks + 3}),
+                        with_values=False)
+    hp = B.HostPlan(w.requests, w.block_table, cfg_for(w), B.options(**opts))
+    inf = hp.info.as_dict()
+    hp.close()
+    return inf
+
+
+@pytest.mark.parametrize("kv,build", [(7 * 128, 0), (8 * 128, 1), (8 * 128 + 1, 1),
+                                      (4 * 128, 0)])
+def test_copies_build_from_8_key_tiles(L, kv, build):
+    # one-row CTAs (MHA decodes): the build that spreads a row's keys over 4
+    # copies is chosen when most key tiles sit in CTAs of >= 8 tiles of 128
+    inf = _host_info([(1, kv)] * 3, dict(kv_chunk=8192), n_q_heads=4, n_kv_heads=4,
+                     head_dim=128, page_size=16)
+    assert inf["n_decode_items"] == 3 * 4
+    assert inf["splitkv_copies"] == build
+
+
+def test_copies_build_needs_at_most_32_rows(L):
+    # 48 rows per CTA (12 new rows x 4 query heads): one thread per row
+    inf = _host_info([(12, 4000)], dict(kv_chunk=8192, prefill_min_rows=-1), n_q_heads=8,
+                     n_kv_heads=2, head_dim=128, page_size=64)
+    assert inf["splitkv_max_rows"] == 48 and inf["splitkv_copies"] == 0
+
+
 @pytest.mark.parametrize("name,rows", [("decode_heavy_gqa4", 4), ("spec_decode_k3", 16),
                                        ("shared_prefix_decode", 24),
                                        ("llama2_7b_orca_iteration", 1)])
