@@ -351,3 +351,42 @@ def test_positions_follow_the_triples(L):
     bad = np.array([[0, 3, 2]], np.int32)  # q_rows > kv_length
     out = np.empty(3, np.int32)
     assert L.mb_positions(bad.ctypes.data, 1, out.ctypes.data, 3) == MB_ERR_SHAPE
+
+# ctypes mirrors of the public structs against the C headers, field by field
+_MIRRORS = [("mb_request_t", "Request"), ("mb_config_t", "Config"),
+            ("mb_plan_options_t", "PlanOptions"), ("mb_plan_info_t", "PlanInfo"),
+            ("mb_sched_config_t", "SchedConfig"), ("mb_sched_stats_t", "SchedStats")]
+
+
+def test_binding_structs_match_the_headers(tmp_path):
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda_inc = next((d for d in ("/usr/local/cuda/include",
+                                 os.path.join(os.environ.get("CUDA_HOME", ""), "include"))
+                     if d and os.path.exists(os.path.join(d, "cuda_runtime_api.h"))), None)
+    if cc is None or cuda_inc is None:
+        pytest.skip("no C compiler or CUDA headers")
+    lines = []
+    for c_name, py_name in _MIRRORS:
+        cls = getattr(B, py_name)
+        lines.append(f'  printf("{py_name} size %zu\\n", sizeof({c_name}));')
+        for f, _ in cls._fields_:
+            lines.append(f'  printf("{py_name} {f} %zu\\n", offsetof({c_name}, {f}));')
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "mb.h"\n#include "mb_sched.h"\n'
+                   "int main(void) {\n" + "\n".join(lines) + "\n  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(root, "include"), "-I", cuda_inc,
+                    str(src), "-o", str(exe)], check=True, capture_output=True)
+    got = {}
+    for ln in subprocess.run([str(exe)], check=True, capture_output=True,
+                             text=True).stdout.splitlines():
+        name, field, val = ln.split()
+        got[(name, field)] = int(val)
+    for _, py_name in _MIRRORS:
+        cls = getattr(B, py_name)
+        assert got[(py_name, "size")] == ctypes.sizeof(cls), py_name
+        for f, _ in cls._fields_:
+            assert got[(py_name, f)] == getattr(cls, f).offset, (py_name, f)
