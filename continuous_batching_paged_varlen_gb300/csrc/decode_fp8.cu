@@ -945,12 +945,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ============================================================================
 // Few-row form: S^T = K Q^T and O^T = V'^T P^T.
 //
-// A CTA of at most 32 query rows (a decode step's g query heads, a
-// speculative step's (k + 1) g rows, a cascade group's sharers) leaves most
-// of a 128-row MMA idle, and the form above pays for that in its per-tile
-// chain: each softmax copy loads, scales and exponentiates 32 scores in a
-// row, with 4 of a warp's 32 lanes busy. Here the tile's 128 keys are the
-// MMA's M and the rows its N (16):
+// A CTA of a few query rows (a decode step's g query heads: at most 8 rows
+// here) leaves most of a 128-row MMA idle, and the form above pays for that
+// in its per-tile chain: each softmax copy loads, scales and exponentiates
+// 32 scores in a row, with 4 of a warp's 32 lanes busy. Here the tile's 128
+// keys are the MMA's M and the rows its N (16):
 //   * S^T[key][n] = sum_d kcode[key][d] qcode[n][d]: kind::f8f6f4 with the
 //     K tile as A (the TMA box already is the K-major swizzled layout) and
 //     Q's code rows as B, in shared memory: the R rows' hi codes in columns
